@@ -1,0 +1,391 @@
+"""QSA benchmark: prefill tokens/s at 128K context and decode us/step at 256K x 64.
+
+One step = one pass of the whole QSA hot path over one batch of synthetic input:
+  prefill (drift_prefill_128k): key compression, indexer scores + top-k_B
+      selection, sparse GQA attention for all 131072 rows of one sequence;
+  decode (decode_256k_x64): block selection + sparse attention for one new
+      token in each of 64 sequences with a 262144-token cache.
+Inputs are resident in HBM when the timed region starts.  `value` is prefill
+tokens/s (all ranks); the decode step time is reported beside it.  `e2e`
+repeats the same step through the public binding with host buffers: the step's
+inputs are copied from pinned host memory and its outputs read back inside the
+timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qsa|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "QSA prefill tokens/s at 128K and decode µs/step at 256K ctx (1×B300)"
+PREFILL = "drift_prefill_128k"
+DECODE = "decode_256k_x64"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d["bf16_tflops_sustained"], "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def prefill_work(n: int, r: int, k_b: int, hq: int, hkv: int, d: int = 128, h_idx: int = 4) -> dict:
+    """Exact algorithmic work of one QSA prefill of n tokens (one sequence)."""
+    i = __import__("numpy").arange(n, dtype="int64")
+    c = (i + 1) // r
+    sel = c.clip(max=k_b)
+    t = sel * r + (i + 1 - c * r)
+    sum_c, sum_t = int(c.sum()), int(t.sum())
+    return {
+        "sum_c": sum_c, "sum_t": sum_t,
+        "index_flops": 2 * h_idx * d * sum_c,
+        "attn_flops": 4 * d * hq * sum_t,
+        "attn_gather_bytes": sum_t * hkv * 2 * d * 2,
+        "compress_bytes": n * d * 2 + (n // r) * d * 2,
+    }
+
+
+def decode_work(batch: int, cache_len: int, r: int, k_b: int, hq: int, hkv: int, d: int = 128,
+                h_idx: int = 4) -> dict:
+    c = cache_len // r
+    t = min(c, k_b) * r + (cache_len - c * r)
+    kbar_bytes = c * d * 2
+    gather = t * hkv * 2 * d * 2
+    small = h_idx * d * 2 + hq * d * 2 * 2 + k_b * 4  # new q_idx, q, out, idx
+    return {"bytes": batch * (kbar_bytes + gather + small), "kbar_bytes": batch * kbar_bytes,
+            "gather_bytes": batch * gather, "tokens": t}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.proc = None
+        self.bus_id = bus_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def bus_id_of(dev) -> str | None:
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_timing(pre_spec, dec_spec, rows_per_step: int, steps: int, seed: int = 0) -> dict:
+    """Times the CPU oracle, as it stands, on a bounded sample of both workloads.
+
+    Prefill: key compression of the whole sequence plus `rows_per_step` query rows
+    at stratified positions (indexer scores, selection, attention), extrapolated to
+    all n rows by the mean row cost.  Decode: one sequence's step, times the batch.
+    """
+    import numpy as np
+    import torch
+    from threadpoolctl import threadpool_info
+
+    from block_sparse_long_17_b300.workloads import make_decode, make_prefill
+    from oracle import qsa_oracle as O
+
+    n, r = pre_spec.n, pre_spec.r
+    wl = make_prefill(pre_spec, "cpu")
+    f32 = lambda t: t.float().numpy()
+    q_idx, k_idx, q, k, v = f32(wl["q_idx"][0]), wl["k_idx"][0].double().numpy(), f32(wl["q"][0]), f32(wl["k"][0]), f32(wl["v"][0])
+    dw = make_decode(dec_spec, "cpu", batch=1)
+    rng = np.random.default_rng(seed)
+    pre_times, dec_times = [], []
+    for s in range(steps):
+        t0 = time.perf_counter()
+        kbar = O.compress_keys(k_idx, r, rope_dims=pre_spec.rope_dims, rope_base=pre_spec.rope_base)
+        t1 = time.perf_counter()
+        strata = (np.arange(rows_per_step) + rng.random(rows_per_step)) / rows_per_step
+        rows = sorted({int(x) for x in (strata * n).astype(np.int64)})
+        O.prefill_rows(q_idx, None, q, k, v, rows, r=r, k_tokens=pre_spec.k_tokens, kbar=kbar)
+        t2 = time.perf_counter()
+        pre_times.append((t1 - t0) + (t2 - t1) / len(rows) * n)
+        t3 = time.perf_counter()
+        O.decode_rows(dw["q_idx"][0, 0].double().numpy(), dw["q"][0, 0].double().numpy(),
+                      dw["kbar"][0].float().numpy(), dw["k"][0].float().numpy(), dw["v"][0].float().numpy(),
+                      dw["cache_len"], r=dec_spec.r, k_tokens=dec_spec.k_tokens)
+        dec_times.append((time.perf_counter() - t3) * dec_spec.batch)
+    threads = max([p.get("num_threads", 1) for p in threadpool_info()] + [1])
+    return {"prefill_s": statistics.mean(pre_times), "decode_s": statistics.mean(dec_times),
+            "cores": threads,
+            "sample": (f"per step: compress all {n // r} blocks + {rows_per_step} of {n} prefill rows "
+                       f"(stratified), extrapolated by mean row cost; decode: 1 of {dec_spec.batch} "
+                       f"sequences x {dec_spec.batch}")}
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["qsa", "reference"], default="qsa")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    import torch
+    from block_sparse_long_17_b300.workloads import WORKLOADS
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    pspec, dspec = WORKLOADS[PREFILL], WORKLOADS[DECODE]
+    pk = peaks()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        steps = max(args.steps, 1)
+        ot = oracle_timing(pspec, dspec, rows_per_step=2, steps=steps)
+        val = pspec.n / ot["prefill_s"]
+        line = {"metric": METRIC, "value": val, "unit": "tokens/s", "impl": "reference",
+                "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+                "ms_per_step": (ot["prefill_s"] + ot["decode_s"]) * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "decode_us_per_step": ot["decode_s"] * 1e6,
+                "config": {"workload": f"{PREFILL} + {DECODE}", "prefill_tokens": pspec.n,
+                           "decode_batch": dspec.batch, "decode_ctx": dspec.ctx, "K": pspec.k_tokens,
+                           "r": pspec.r},
+                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": ot["cores"], "kind": "oracle",
+                                 "sample": ot["sample"]},
+                "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    from block_sparse_long_17_b300 import qsa
+    from block_sparse_long_17_b300.workloads import make_decode, make_prefill
+
+    qsa.load_library()  # raises if the CUDA library is missing: no fallback path exists
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+
+    cfg = qsa.Config(r=pspec.r, k_tokens=pspec.k_tokens, rope_dims=pspec.rope_dims, rope_base=pspec.rope_base)
+    wl = make_prefill(pspec, dev)
+    pre = qsa.QsaPrefill(cfg, 1, pspec.n, pspec.hq, pspec.hkv, device=dev)
+    dwl = make_decode(dspec, dev)
+    dcfg = qsa.Config(r=dspec.r, k_tokens=dspec.k_tokens, rope_dims=dspec.rope_dims, rope_base=dspec.rope_base)
+    dec = qsa.QsaDecode(dcfg, dspec.batch, dwl["n_blocks"], dspec.hq, dspec.hkv, device=dev)
+    dq = dwl["q"][:, 0].contiguous()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    names = ["compress", "index_prefill", "attn_prefill", "index_decode", "attn_decode"]
+
+    def step(evs):
+        evs[0].record(stream)
+        qsa.qsa_compress_keys(cfg, wl["k_idx"], 0, pre.n_blocks, pre.kbar)
+        evs[1].record(stream)
+        qsa.qsa_index_topk(cfg, wl["q_idx"], pre.kbar, pre.q_pos, pre.n_blocks, pre.idx, pre.count, pre.ws)
+        evs[2].record(stream)
+        qsa.qsa_sparse_attn_prefill(cfg, wl["q"], wl["k"], wl["v"], pre.q_pos, pre.idx, pre.count,
+                                    pre.out, pre.lse)
+        evs[3].record(stream)
+        q_pos = dwl["cache_lens"] - 1
+        qsa.qsa_index_topk(dcfg, dwl["q_idx"], dwl["kbar"], q_pos, dwl["n_blocks"], dec.idx, dec.count, dec.ws_idx)
+        evs[4].record(stream)
+        qsa.qsa_sparse_attn_decode(dcfg, dq, dwl["k"], dwl["v"], dwl["cache_lens"], dec.idx.view(dspec.batch, -1),
+                                   dec.count.view(dspec.batch), dec.out, dec.ws_attn, dec.lse)
+        evs[5].record(stream)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(mk())
+    torch.cuda.synchronize()
+    assert qsa.qsa_read_device_error() == 0
+
+    clocks = ClockSampler(bus_id_of(dev))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = qsa.qsa_launch_count()
+    all_evs = []
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()  # L2 flush between steps, outside the step's events
+        evs = mk()
+        step(evs)
+        all_evs.append(evs)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    launches = (qsa.qsa_launch_count() - launches0) // args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+
+    parts = {nm: [] for nm in names}
+    for evs in all_evs:
+        for j, nm in enumerate(names):
+            parts[nm].append(evs[j].elapsed_time(evs[j + 1]))
+    mean = {nm: statistics.mean(v) for nm, v in parts.items()}
+    prefill_ms = mean["compress"] + mean["index_prefill"] + mean["attn_prefill"]
+    decode_ms = mean["index_decode"] + mean["attn_decode"]
+    step_ms = prefill_ms + decode_ms
+    t = torch.tensor([prefill_ms, decode_ms, step_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    prefill_ms, decode_ms, step_ms = t.tolist()
+    value = world * pspec.n / (prefill_ms * 1e-3)
+
+    # Roofline of each part (algorithmic work / measured mean duration).
+    pw = prefill_work(pspec.n, pspec.r, pspec.k_b, pspec.hq, pspec.hkv)
+    dwk = decode_work(dspec.batch, dwl["cache_len"], dspec.r, dspec.k_b, dspec.hq, dspec.hkv)
+    hbm = pk["hbm_gbs"]
+    roofs = {
+        "compress": {"bound": "hbm", "achieved": pw["compress_bytes"] / (mean["compress"] * 1e-3) / 1e9,
+                     "peak": hbm, "unit": "GB/s"},
+        "index_prefill": {"bound": "tensor", "achieved": pw["index_flops"] / (mean["index_prefill"] * 1e-3) / 1e12,
+                          "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s"},
+        "attn_prefill": {"bound": "hbm", "achieved": pw["attn_gather_bytes"] / (mean["attn_prefill"] * 1e-3) / 1e9,
+                         "peak": hbm, "unit": "GB/s"},
+        "decode": {"bound": "hbm", "achieved": dwk["bytes"] / (decode_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s"},
+    }
+    for v in roofs.values():
+        v["frac"] = v["achieved"] / v["peak"]
+    dominant = max(["compress", "index_prefill", "attn_prefill"], key=lambda nm: mean[nm])
+    roof = dict(roofs[dominant])
+    roof["kernel"] = dominant
+    roof["traffic"] = None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "decode_us_per_step": decode_ms * 1e3,
+        "prefill_ms": prefill_ms,
+        "parts_ms": mean,
+        "config": {"workload": f"{PREFILL} + {DECODE}", "prefill_tokens": pspec.n, "prefill_batch": 1,
+                   "decode_batch": dspec.batch, "decode_ctx": dspec.ctx, "K": pspec.k_tokens, "r": pspec.r,
+                   "Hq": pspec.hq, "Hkv": pspec.hkv, "H_idx": pspec.h_idx, "d": pspec.d,
+                   "l2": "256 MiB buffer written between steps, outside the timed events",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof, "rooflines": roofs, "peaks_source": pk["source"],
+        "gpu_launches": int(launches), "clocks": clk, "wall_s_timed": wall,
+    }
+
+    if not args.no_e2e and rank == 0:
+        line["e2e"] = e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev)
+    if not args.no_cpu_baseline and rank == 0:
+        ot = oracle_timing(pspec, dspec, rows_per_step=3, steps=1)
+        line["cpu_baseline"] = {"value": pspec.n / ot["prefill_s"], "unit": "tokens/s", "cores": ot["cores"],
+                                "kind": "oracle", "sample": ot["sample"],
+                                "decode_us_per_step": ot["decode_s"] * 1e6}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev) -> dict:
+    """The same step through the binding with host buffers: H2D of the step's inputs
+    from pinned memory and D2H of its outputs, all inside the timed region."""
+    import torch
+    host_in = {k: wl[k].cpu().pin_memory() for k in ("q_idx", "k_idx", "q", "k", "v")}
+    dev_in = {k: torch.empty_like(wl[k]) for k in host_in}
+    dq_h = dwl["q"][:, 0].contiguous().cpu().pin_memory()
+    dqi_h = dwl["q_idx"].cpu().pin_memory()
+    dq_d, dqi_d = torch.empty_like(dq_h, device=dev), torch.empty_like(dqi_h, device=dev)
+    out_h = torch.empty(pre.out.shape, dtype=pre.out.dtype).pin_memory()
+    dout_h = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + dq_h.numel() * 2 + dqi_h.numel() * 2
+    d2h = out_h.numel() * 2 + dout_h.numel() * 2
+
+    def one():
+        for k in host_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        dq_d.copy_(dq_h, non_blocking=True)
+        dqi_d.copy_(dqi_h, non_blocking=True)
+        qsa.qsa_compress_keys(cfg, dev_in["k_idx"], 0, pre.n_blocks, pre.kbar)
+        qsa.qsa_index_topk(cfg, dev_in["q_idx"], pre.kbar, pre.q_pos, pre.n_blocks, pre.idx, pre.count, pre.ws)
+        qsa.qsa_sparse_attn_prefill(cfg, dev_in["q"], dev_in["k"], dev_in["v"], pre.q_pos, pre.idx, pre.count,
+                                    pre.out, pre.lse)
+        out_h.copy_(pre.out, non_blocking=True)
+        q_pos = dwl["cache_lens"] - 1
+        qsa.qsa_index_topk(dcfg, dqi_d, dwl["kbar"], q_pos, dwl["n_blocks"], dec.idx, dec.count, dec.ws_idx)
+        qsa.qsa_sparse_attn_decode(dcfg, dq_d, dwl["k"], dwl["v"], dwl["cache_lens"], dec.idx.view(dspec.batch, -1),
+                                   dec.count.view(dspec.batch), dec.out, dec.ws_attn, dec.lse)
+        dout_h.copy_(dec.out, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k = max(1, min(args.steps, 3))
+    e0.record(stream)
+    for _ in range(k):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / k
+    return {"value": wl["q"].shape[1] / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "note": "tokens/s of the prefill sequence over the whole step incl. copies and decode"}
+
+
+if __name__ == "__main__":
+    main()

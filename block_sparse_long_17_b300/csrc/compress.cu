@@ -1,0 +1,133 @@
+// Key compression and query rotation for the QSA indexer.
+//
+// "On the Design of Qwen3.8-Next Architecture", research-hub notes, Key ideas,
+// QSA compressed-indexer bullet: keys are average-pooled into blocks of r and get
+// partial RoPE (64 of 128 dims) after compression.  paperglide reader, "Qwen
+// Sparse Attention" step 2: the pooled key may pass through RMSNorm (optional
+// here, unit weight).  Both operations are memory-bound: one warp per output row,
+// 16-byte-friendly coalesced reads, fp32 arithmetic with fp64 RoPE angles, and a
+// single round to bf16.
+#include "common.cuh"
+
+namespace qsa {
+
+constexpr int kCompressWarps = 8;
+
+// One warp per compressed block.  Lane l owns dims {l, l+32, l+64, l+96} while
+// pooling; the pooled fp32 row is staged in shared memory so that any even
+// rope_dims can pair dim j with dim j + rope_dims/2.
+__global__ void __launch_bounds__(kCompressWarps * 32)
+compress_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_t k_stride_b, int64_t B,
+                     int64_t first_block, int64_t n_blocks, int r, int rmsnorm, float rms_eps,
+                     RopeParams rope, __nv_bfloat16* __restrict__ kbar, int64_t kbar_stride_b) {
+  __shared__ float pooled[kCompressWarps][kHeadDim];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * kCompressWarps + warp;
+  if (item >= B * n_blocks) return;
+  const int64_t bb = item / n_blocks;
+  const int64_t blk = first_block + item % n_blocks;
+  const __nv_bfloat16* src = k_idx + bb * k_stride_b + blk * r * kHeadDim;
+
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int t = 0; t < r; ++t) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] += __bfloat162float(src[t * kHeadDim + lane + 32 * u]);
+  }
+  const float inv_r = 1.0f / (float)r;  // r is a power of two: exact
+#pragma unroll
+  for (int u = 0; u < 4; ++u) acc[u] *= inv_r;
+  if (rmsnorm) {
+    float ss = acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = rsqrtf(ss * (1.0f / kHeadDim) + rms_eps);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) acc[u] *= inv;
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) pooled[warp][lane + 32 * u] = acc[u];
+  __syncwarp();
+
+  __nv_bfloat16* dst = kbar + bb * kbar_stride_b + blk * kHeadDim;
+  const int half = rope.half;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int dim = lane + 32 * u;
+    float y = pooled[warp][dim];
+    if (dim < 2 * half) {
+      const int j = dim < half ? dim : dim - half;
+      float c, s;
+      rope_cos_sin(blk, rope.theta[j], &c, &s);
+      const float x1 = pooled[warp][j], x2 = pooled[warp][j + half];
+      y = dim < half ? fmaf(x1, c, -x2 * s) : fmaf(x1, s, x2 * c);
+    }
+    dst[dim] = __float2bfloat16_rn(y);
+  }
+}
+
+// One warp per query token: the RoPE angles of position floor(i / r) are
+// computed once per token and applied to all four indexer heads.
+__global__ void __launch_bounds__(kCompressWarps * 32)
+rotate_queries_kernel(const __nv_bfloat16* __restrict__ q_idx, const int64_t* __restrict__ q_pos,
+                      int64_t B, int64_t n_q, int r, RopeParams rope,
+                      __nv_bfloat16* __restrict__ qt) {
+  __shared__ float cs[kCompressWarps][2][kMaxRopePairs];
+  __shared__ float row[kCompressWarps][kHeadDim];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * kCompressWarps + warp;
+  if (item >= B * n_q) return;
+  const int64_t bb = item / n_q;
+  const int64_t pos = (q_pos[bb] + item % n_q) / r;
+  const int half = rope.half;
+  for (int j = lane; j < half; j += 32) {
+    float c, s;
+    rope_cos_sin(pos, rope.theta[j], &c, &s);
+    cs[warp][0][j] = c;
+    cs[warp][1][j] = s;
+  }
+  const __nv_bfloat16* src = q_idx + item * (kIdxHeads * kHeadDim);
+  __nv_bfloat16* dst = qt + item * (kIdxHeads * kHeadDim);
+  for (int h = 0; h < kIdxHeads; ++h) {
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) row[warp][lane + 32 * u] = __bfloat162float(src[h * kHeadDim + lane + 32 * u]);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int dim = lane + 32 * u;
+      float y = row[warp][dim];
+      if (dim < 2 * half) {
+        const int j = dim < half ? dim : dim - half;
+        const float c = cs[warp][0][j], s = cs[warp][1][j];
+        const float x1 = row[warp][j], x2 = row[warp][j + half];
+        y = dim < half ? fmaf(x1, c, -x2 * s) : fmaf(x1, s, x2 * c);
+      }
+      dst[h * kHeadDim + dim] = __float2bfloat16_rn(y);
+    }
+  }
+}
+
+cudaError_t launch_compress_keys(const __nv_bfloat16* k_idx, int64_t k_stride_b, int64_t B,
+                                 int64_t first_block, int64_t n_blocks, int r, int rmsnorm,
+                                 float rms_eps, const RopeParams& rope, __nv_bfloat16* kbar,
+                                 int64_t kbar_stride_b, cudaStream_t st) {
+  const int64_t items = B * n_blocks;
+  if (items == 0) return cudaSuccess;
+  const int64_t grid = (items + kCompressWarps - 1) / kCompressWarps;
+  compress_keys_kernel<<<(unsigned)grid, kCompressWarps * 32, 0, st>>>(
+      k_idx, k_stride_b, B, first_block, n_blocks, r, rmsnorm, rms_eps, rope, kbar, kbar_stride_b);
+  return count_launch(cudaGetLastError());
+}
+
+cudaError_t launch_rotate_queries(const __nv_bfloat16* q_idx, const int64_t* q_pos, int64_t B,
+                                  int64_t n_q, int r, const RopeParams& rope, __nv_bfloat16* qt,
+                                  cudaStream_t st) {
+  const int64_t items = B * n_q;
+  if (items == 0) return cudaSuccess;
+  const int64_t grid = (items + kCompressWarps - 1) / kCompressWarps;
+  rotate_queries_kernel<<<(unsigned)grid, kCompressWarps * 32, 0, st>>>(q_idx, q_pos, B, n_q, r,
+                                                                         rope, qt);
+  return count_launch(cudaGetLastError());
+}
+
+}  // namespace qsa

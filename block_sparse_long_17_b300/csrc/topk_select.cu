@@ -1,0 +1,182 @@
+// Exact top-k_B block selection over a stored score row.
+//
+// "On the Design of Qwen3.8-Next Architecture", research-hub notes, Key ideas,
+// QSA compressed-indexer bullet: each query keeps the top k_B = ceil(K / r)
+// blocks; paperglide reader, "Qwen Sparse Attention" step 4 (top-K_B per query,
+// expanded back to token indices).  Equal scores go to the lower block id.
+//
+// One CTA per row.  Scores are ReLU sums, so their fp32 bit patterns (sign
+// cleared) order exactly like the values.  A radix descent narrows the range
+// [lo, hi] of bit patterns that holds the k_B-th largest score: each pass builds
+// a 2048-bin histogram of the patterns inside the range and keeps the bin where
+// the running count from the top crosses the number still needed.  It ends when
+// that bin holds exactly the number needed, or when it is a single value (an
+// exact tie, resolved by taking the lowest block ids first).  A final ordered
+// compaction writes the winners in ascending block order.
+#include "common.cuh"
+
+namespace qsa {
+
+constexpr int kSelThreads = 512;
+constexpr int kSelBins = 2048;
+constexpr int kSelBinsPerThread = kSelBins / kSelThreads;
+
+__device__ __forceinline__ uint32_t score_key(float s) { return __float_as_uint(s) & 0x7fffffffu; }
+
+// Exclusive scan of `v` across the CTA (blockDim = kSelThreads); returns the
+// prefix and stores the total in *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kSelThreads / 32 ? warp_sums[lane] : 0;
+    int inc = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane < kSelThreads / 32) warp_sums[lane] = inc - w;
+    if (lane == 31) *total = inc;
+  }
+  __syncthreads();
+  const int r = warp_sums[warp] + x - v;
+  __syncthreads();
+  return r;
+}
+
+// S: [n_rows][s_stride] fp32 (row j of this launch is global row row_lo + j);
+// idx: [rows][k_b]; count: [rows].
+__global__ void __launch_bounds__(kSelThreads)
+topk_select_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t* __restrict__ q_pos,
+                   int64_t n_q, int64_t row_lo, int r, int k_b, int64_t c_cap,
+                   int32_t* __restrict__ idx, int32_t* __restrict__ count) {
+  __shared__ int hist[kSelBins];
+  __shared__ int warp_sums[32];
+  __shared__ int sh_total;
+  __shared__ uint32_t sh_lo, sh_hi;
+  __shared__ int sh_need, sh_done;
+
+  const int64_t row = row_lo + blockIdx.x;
+  const int64_t bb = row / n_q;
+  const int64_t pos = q_pos[bb] + row % n_q;
+  int64_t c = (pos + 1) / r;
+  if (c > c_cap) c = c_cap;  // reported by the scan kernel
+  int32_t* out = idx + row * (int64_t)k_b;
+  if (c <= k_b) {
+    for (int j = threadIdx.x; j < k_b; j += kSelThreads) out[j] = j < c ? j : -1;
+    if (threadIdx.x == 0) count[row] = (int32_t)c;
+    return;
+  }
+  const float* s = S + (int64_t)blockIdx.x * s_stride;
+
+  // done = 1: winners are key > hi plus every key in [lo, hi];
+  // done = 2: lo == hi, winners are key > hi plus the first `need` keys == lo.
+  uint32_t lo = 0, hi = 0x7fffffffu;
+  int need = k_b, done = 0;
+  while (!done) {
+    const uint32_t width = hi - lo;
+    const int nbits = 32 - __clz(width);
+    const int shift = nbits > 11 ? nbits - 11 : 0;
+    for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) hist[j] = 0;
+    __syncthreads();
+    for (int64_t e = threadIdx.x; e < c; e += kSelThreads) {
+      const uint32_t u = score_key(s[e]);
+      if (u >= lo && u <= hi) atomicAdd(&hist[(u - lo) >> shift], 1);
+    }
+    __syncthreads();
+    // Counts from the top: thread j owns bins [4(T-1-j), 4(T-1-j)+4) so that the
+    // exclusive scan over threads is a suffix sum over bins.
+    const int base_bin = (kSelThreads - 1 - threadIdx.x) * kSelBinsPerThread;
+    int loc[kSelBinsPerThread];
+    int sum = 0;
+#pragma unroll
+    for (int q = 0; q < kSelBinsPerThread; ++q) {
+      loc[q] = hist[base_bin + kSelBinsPerThread - 1 - q];  // descending bins
+      sum += loc[q];
+    }
+    const int above0 = block_exclusive_scan(sum, warp_sums, &sh_total);
+    if (above0 < need && above0 + sum >= need) {
+      int above = above0;
+#pragma unroll
+      for (int q = 0; q < kSelBinsPerThread; ++q) {
+        if (above + loc[q] >= need) {
+          const int bin = base_bin + kSelBinsPerThread - 1 - q;
+          const uint32_t nlo = lo + ((uint32_t)bin << shift);
+          const uint32_t span = shift >= 32 ? 0xffffffffu : ((1u << shift) - 1u);
+          const uint32_t nhi = (hi - nlo) < span ? hi : nlo + span;
+          const int nneed = need - above;
+          sh_lo = nlo;
+          sh_hi = nhi;
+          sh_need = nneed;
+          sh_done = (loc[q] == nneed) ? 1 : (nlo == nhi ? 2 : 0);
+          break;
+        }
+        above += loc[q];
+      }
+    }
+    __syncthreads();
+    lo = sh_lo;
+    hi = sh_hi;
+    need = sh_need;
+    done = sh_done;
+    __syncthreads();
+  }
+
+  // Ordered compaction: each thread takes 4 consecutive blocks per round.
+  int written = 0, ties_taken = 0;
+  for (int64_t e0 = 0; e0 < c; e0 += 4 * kSelThreads) {
+    const int64_t e = e0 + 4 * threadIdx.x;
+    uint32_t win = 0, tie = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (e + q < c) {
+        const uint32_t u = score_key(s[e + q]);
+        if (u > hi || (done == 1 && u >= lo)) win |= 1u << q;
+        else if (done == 2 && u == lo) tie |= 1u << q;
+      }
+    }
+    const int n_tie = __popc(tie);
+    const int tie_before = ties_taken + block_exclusive_scan(n_tie, warp_sums, &sh_total);
+    const int tie_total = sh_total;
+    // Ties are taken in block order while the quota lasts.
+#pragma unroll
+    for (int q = 0, k = 0; q < 4; ++q) {
+      if (tie & (1u << q)) {
+        if (tie_before + k < need) win |= 1u << q;
+        ++k;
+      }
+    }
+    ties_taken += tie_total;
+    const int n_win = __popc(win);
+    const int before = written + block_exclusive_scan(n_win, warp_sums, &sh_total);
+    const int win_total = sh_total;
+#pragma unroll
+    for (int q = 0, k = 0; q < 4; ++q) {
+      if (win & (1u << q)) {
+        if (before + k < k_b) out[before + k] = (int32_t)(e + q);  // exactly k_b winners exist
+        ++k;
+      }
+    }
+    written += win_total;
+  }
+  if (threadIdx.x == 0) count[row] = k_b;
+}
+
+cudaError_t launch_topk_select(const float* S, int64_t s_stride, const int64_t* q_pos, int64_t n_q,
+                               int64_t row_lo, int64_t n_rows, int r, int k_b, int64_t c_cap,
+                               int32_t* idx, int32_t* count, cudaStream_t st) {
+  if (n_rows <= 0) return cudaSuccess;
+  topk_select_kernel<<<(unsigned)n_rows, kSelThreads, 0, st>>>(S, s_stride, q_pos, n_q, row_lo, r,
+                                                               k_b, c_cap, idx, count);
+  return count_launch(cudaGetLastError());
+}
+
+}  // namespace qsa

@@ -1,0 +1,305 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the CPU oracle
+on identical seeded inputs.
+
+Selections must match the oracle exactly except at near-ties (see
+qsa_check.check_selection_row); attention outputs must be within 1e-2 max-abs
+of the fp64 oracle for unit-variance V.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_long_17_b300 import qsa
+from block_sparse_long_17_b300.workloads import WORKLOADS, DecodeSpec, PrefillSpec, make_decode, make_prefill
+from oracle import qsa_oracle as O
+from tests import qsa_check as QC
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def cfg_for(spec, **kw) -> qsa.Config:
+    base = dict(r=spec.r, rope_dims=spec.rope_dims, rope_base=spec.rope_base, k_tokens=spec.k_tokens)
+    base.update(kw)
+    return qsa.Config(**base)
+
+
+def run_prefill(cfg: qsa.Config, wl: dict, q_pos0: int = 0, rows: slice | None = None):
+    """Full GPU prefill of sequence batch `wl` through the binding; returns numpy views."""
+    q_idx, k_idx, q, k, v = wl["q_idx"], wl["k_idx"], wl["q"], wl["k"], wl["v"]
+    if rows is not None:  # chunk of query rows at positions q_pos0 + j
+        q_idx, q = q_idx[:, rows].contiguous(), q[:, rows].contiguous()
+    B, n_q = q_idx.shape[0], q_idx.shape[1]
+    L = k_idx.shape[1]
+    nb = L // cfg.r
+    kbar = torch.empty((B, max(nb, 1), 128), dtype=torch.bfloat16, device=DEV)
+    qsa.qsa_compress_keys(cfg, k_idx, 0, nb, kbar)
+    q_pos = torch.full((B,), q_pos0, dtype=torch.int64, device=DEV)
+    idx = torch.empty((B, n_q, cfg.k_b), dtype=torch.int32, device=DEV)
+    cnt = torch.empty((B, n_q), dtype=torch.int32, device=DEV)
+    ws = torch.empty((qsa.qsa_index_topk_workspace(cfg, B, n_q, nb),), dtype=torch.uint8, device=DEV)
+    qsa.qsa_index_topk(cfg, q_idx, kbar, q_pos, nb, idx, cnt, ws)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=DEV)
+    qsa.qsa_sparse_attn_prefill(cfg, q, k, v, q_pos, idx, cnt, out, lse)
+    torch.cuda.synchronize()
+    assert qsa.qsa_read_device_error() == 0
+    return {"kbar": kbar, "idx": idx.cpu().numpy(), "count": cnt.cpu().numpy(),
+            "out": out.float().cpu().numpy(), "lse": lse.cpu().numpy()}
+
+
+# ----------------------------------------------------------------------------- key compression
+
+@pytest.mark.parametrize("r,rope_dims,rmsnorm,n", [(4, 64, False, 2048), (4, 64, True, 2048),
+                                                    (2, 64, False, 999), (8, 128, False, 1030),
+                                                    (16, 32, True, 517), (4, 0, False, 64)])
+def test_compress_keys_matches_oracle(r, rope_dims, rmsnorm, n):
+    spec = PrefillSpec("t", n=n, k_tokens=64, seed=11, r=r, rope_dims=rope_dims)
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec, rmsnorm=rmsnorm)
+    nb = n // r
+    kbar = torch.zeros((1, nb, 128), dtype=torch.bfloat16, device=DEV)
+    qsa.qsa_compress_keys(cfg, wl["k_idx"], 0, nb, kbar)
+    ref = O.compress_keys(QC.bf16_to_np(wl["k_idx"][0]), r, rope_dims=rope_dims,
+                          rope_base=cfg.rope_base, rmsnorm=rmsnorm, rms_eps=cfg.rms_eps)
+    ref_t = torch.from_numpy(ref).to(torch.bfloat16)  # exact: ref values are bf16 numbers
+    d = QC.ulp_distance_bf16(kbar[0].cpu(), ref_t)
+    assert d.max() <= 1, "kbar off by more than one bf16 ulp"
+    assert (d > 0).mean() < 1e-3, f"too many 1-ulp differences: {(d > 0).mean()}"
+
+
+def test_compress_keys_decode_append_touches_only_its_block():
+    spec = DecodeSpec("t", batch=3, ctx=203, k_tokens=64, seed=5)
+    gen = torch.Generator(device=DEV).manual_seed(5)
+    L = 208
+    k_idx = torch.randn((3, L, 128), generator=gen, device=DEV).to(torch.bfloat16)
+    cfg = cfg_for(spec)
+    kbar = torch.full((3, 64, 128), 7.0, dtype=torch.bfloat16, device=DEV)
+    qsa.qsa_compress_keys(cfg, k_idx, 51, 1, kbar)  # block 51 = tokens 204..207
+    kb = kbar.cpu()
+    for bb in range(3):
+        ref = O.compress_keys(QC.bf16_to_np(k_idx[bb]), 4)[51]
+        d = QC.ulp_distance_bf16(kb[bb, 51], torch.from_numpy(ref).to(torch.bfloat16))
+        assert d.max() <= 1
+        assert (kb[bb, :51] == 7.0).all() and (kb[bb, 52:] == 7.0).all()
+
+
+# ----------------------------------------------------------------------------- tiny prefill (cfg 0)
+
+@pytest.fixture(scope="module")
+def tiny():
+    spec = WORKLOADS["tiny_prefill_2k"]
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    gpu = run_prefill(cfg, wl)
+    res = QC.oracle_rows(wl, range(spec.n), cfg=cfg)
+    return spec, cfg, wl, gpu, res
+
+
+def test_tiny_prefill_selection_and_output_all_rows(tiny):
+    spec, cfg, wl, gpu, res = tiny
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0],
+                            cfg.k_b, cfg.r)
+    assert st["exact"] + st["margin"] == spec.n
+    assert st["margin"] <= spec.n // 100, st
+
+
+def test_tiny_attention_on_oracle_selection(tiny):
+    """The attention kernel alone, fed the oracle's own selection, on every row."""
+    spec, cfg, wl, gpu, res = tiny
+    n, k_b = spec.n, cfg.k_b
+    idx = np.full((1, n, k_b), -1, dtype=np.int32)
+    cnt = np.zeros((1, n), dtype=np.int32)
+    for j in range(n):
+        s = res["sel"][j]
+        idx[0, j, :len(s)] = s
+        cnt[0, j] = len(s)
+    q_pos = torch.zeros((1,), dtype=torch.int64, device=DEV)
+    out = torch.empty_like(wl["q"])
+    lse = torch.empty(wl["q"].shape[:3], dtype=torch.float32, device=DEV)
+    qsa.qsa_sparse_attn_prefill(cfg, wl["q"], wl["k"], wl["v"], q_pos, torch.from_numpy(idx).to(DEV),
+                                torch.from_numpy(cnt).to(DEV), out, lse)
+    o = out.float().cpu().numpy()[0]
+    assert np.abs(o - res["out"]).max() <= QC.OUT_ATOL
+    assert np.abs(lse.cpu().numpy()[0] - res["lse"]).max() <= QC.LSE_ATOL
+
+
+def test_tiny_rotated_query_scores_match_oracle(tiny):
+    """Selections agree with the oracle on >= 99% of the rows that must choose."""
+    spec, cfg, wl, gpu, res = tiny
+    choosing = [j for j in range(spec.n) if O.visible_blocks(j, cfg.r) > cfg.k_b]
+    same = sum(np.array_equal(gpu["idx"][0, j, :cfg.k_b], res["sel"][j]) for j in choosing)
+    assert same >= 0.99 * len(choosing)
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def small_case(n, k_tokens, r=4, hq=16, hkv=2, seed=3, rope_dims=64):
+    spec = PrefillSpec("e", n=n, k_tokens=k_tokens, seed=seed, r=r, hq=hq, hkv=hkv, rope_dims=rope_dims)
+    return spec, make_prefill(spec, DEV)
+
+
+@pytest.mark.parametrize("n,k_tokens,r,hq,hkv", [
+    (1, 64, 4, 16, 2),       # one token, no complete block: tail only
+    (3, 64, 4, 16, 2),       # n < r
+    (37, 4096, 4, 16, 2),    # k_B >= every block: dense causal attention
+    (300, 64, 4, 8, 8),      # group size 1 (MHA)
+    (300, 64, 4, 32, 2),     # group size 16: two head chunks per kv head
+    (300, 64, 4, 12, 4),     # group size 3: padded head chunk
+    (401, 40, 2, 16, 2),     # r = 2, k_B = 20
+    (777, 128, 8, 16, 2),    # r = 8
+    (515, 48, 16, 16, 1),    # r = 16, one kv head
+])
+def test_edge_shapes_match_oracle(n, k_tokens, r, hq, hkv):
+    spec, wl = small_case(n, k_tokens, r, hq, hkv)
+    cfg = cfg_for(spec)
+    gpu = run_prefill(cfg, wl)
+    res = QC.oracle_rows(wl, range(n), cfg=cfg)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0],
+                            cfg.k_b, cfg.r)
+    assert st["exact"] >= 0.98 * n
+
+
+def test_dense_limit_equals_torch_sdpa():
+    """k_B >= every block: QSA is dense causal GQA (checked against torch SDPA, fp32)."""
+    spec, wl = small_case(129, 1 << 12)
+    cfg = cfg_for(spec)
+    gpu = run_prefill(cfg, wl)
+    q = wl["q"][0].float().permute(1, 0, 2)[None]
+    k = wl["k"][0].float().repeat_interleave(8, dim=0)[None]
+    v = wl["v"][0].float().repeat_interleave(8, dim=0)[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)[0].permute(1, 0, 2)
+    assert np.abs(gpu["out"][0] - ref.cpu().numpy()).max() <= QC.OUT_ATOL
+
+
+def test_exact_ties_take_lowest_block_ids():
+    """All-zero indexer keys: every score is 0, so the first k_B blocks win."""
+    spec, wl = small_case(300, 64)
+    wl["k_idx"].zero_()
+    cfg = cfg_for(spec)
+    gpu = run_prefill(cfg, wl)
+    for j in range(300):
+        c = O.visible_blocks(j, 4)
+        want = np.arange(min(c, cfg.k_b))
+        np.testing.assert_array_equal(gpu["idx"][0, j, :len(want)], want)
+
+
+def test_planted_block_always_selected():
+    """A key block equal to a row's query direction outranks every random block."""
+    spec, wl = small_case(2048, 256, seed=9)
+    cfg = cfg_for(spec)
+    i, blk = 1500, 100
+    wl["k_idx"][0, 4 * blk:4 * blk + 4] = (wl["q_idx"][0, i, 0].float() * 4).to(torch.bfloat16)
+    gpu = run_prefill(cfg, wl)
+    assert blk in gpu["idx"][0, i, :gpu["count"][0, i]]
+    res = QC.oracle_rows(wl, [i], cfg=cfg)
+    QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, 4)
+
+
+def test_chunked_prefill_rows_at_offset():
+    """A chunk of query rows at positions 1000.. against the whole cached prefix."""
+    spec, wl = small_case(2048, 512, seed=12)
+    cfg = cfg_for(spec)
+    lo, hi = 1000, 1400
+    gpu = run_prefill(cfg, wl, q_pos0=lo, rows=slice(lo, hi))
+    res = QC.oracle_rows({**wl, "q_idx": wl["q_idx"][:, lo:hi], "q": wl["q"][:, lo:hi]},
+                         range(hi - lo), cfg=cfg, q_pos0=lo)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0],
+                            cfg.k_b, cfg.r)
+    assert st["exact"] >= 0.98 * (hi - lo)
+
+
+def test_rmsnorm_variant_end_to_end():
+    spec, wl = small_case(700, 128, seed=13)
+    cfg = cfg_for(spec, rmsnorm=True)
+    gpu = run_prefill(cfg, wl)
+    res = QC.oracle_rows(wl, range(0, 700, 7), cfg=cfg)
+    QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, 4)
+
+
+def test_invalid_selection_reports_instead_of_faulting():
+    spec, wl = small_case(64, 16, seed=14)
+    cfg = cfg_for(spec)
+    q_pos = torch.zeros((1,), dtype=torch.int64, device=DEV)
+    idx = torch.full((1, 64, cfg.k_b), 10 ** 6, dtype=torch.int32, device=DEV)  # out of range ids
+    cnt = torch.full((1, 64), cfg.k_b, dtype=torch.int32, device=DEV)
+    out = torch.empty_like(wl["q"])
+    qsa.qsa_sparse_attn_prefill(cfg, wl["q"], wl["k"], wl["v"], q_pos, idx, cnt, out)
+    assert qsa.qsa_read_device_error() == 1  # QSA_ERR_INVALID_ARG
+    assert qsa.qsa_read_device_error() == 0  # the word is cleared by the read
+    assert torch.isfinite(out.float()).all()
+
+
+# ----------------------------------------------------------------------------- decode
+
+def run_decode(cfg, wl, Hq=16, Hkv=2):
+    B = wl["batch"]
+    dec = qsa.QsaDecode(cfg, B, wl["n_blocks"], Hq, Hkv)
+    out = dec(wl["q_idx"], wl["q"][:, 0].contiguous(), wl["kbar"], wl["k"], wl["v"], wl["cache_lens"])
+    torch.cuda.synchronize()
+    assert qsa.qsa_read_device_error() == 0
+    return dec.idx.view(B, -1).cpu().numpy(), dec.count.view(B).cpu().numpy(), out.float().cpu().numpy(), dec.lse.cpu().numpy()
+
+
+def check_decode_seq(cfg, wl, bb, idx, cnt, out, lse):
+    L = int(wl["cache_lens"][bb])
+    res = O.decode_rows(QC.bf16_to_np(wl["q_idx"][bb, 0]), QC.bf16_to_np(wl["q"][bb, 0]),
+                        QC.bf16_to_np(wl["kbar"][bb]), QC.bf16_to_np(wl["k"][bb]),
+                        QC.bf16_to_np(wl["v"][bb]), L, r=cfg.r, k_tokens=cfg.k_tokens)
+    kind = QC.check_selection_row(res["scores"][0], res["sel"][0], idx[bb], int(cnt[bb]),
+                                  O.visible_blocks(L - 1, cfg.r), cfg.k_b)
+    if kind == "exact":
+        assert np.abs(out[bb] - res["out"][0]).max() <= QC.OUT_ATOL
+        assert np.abs(lse[bb] - res["lse"][0]).max() <= QC.LSE_ATOL
+    return kind
+
+
+@pytest.mark.parametrize("ctx", [2, 100, 2047, 2048, 5003])
+def test_decode_small_matches_oracle(ctx):
+    spec = DecodeSpec("d", batch=3, ctx=ctx, k_tokens=512, seed=21)
+    wl = make_decode(spec, DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode(cfg, wl)
+    kinds = [check_decode_seq(cfg, wl, bb, idx, cnt, out, lse) for bb in range(3)]
+    assert kinds.count("exact") >= 2
+
+
+def test_decode_ragged_cache_lengths():
+    """Sequences of one batch at different lengths (each its own c_i and tail)."""
+    spec = DecodeSpec("d", batch=4, ctx=3000, k_tokens=256, seed=22)
+    wl = make_decode(spec, DEV)
+    wl["cache_lens"] = torch.tensor([3001, 17, 2050, 1203], dtype=torch.int64, device=DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode(cfg, wl)
+    for bb in range(4):
+        check_decode_seq(cfg, wl, bb, idx, cnt, out, lse)
+
+
+@pytest.mark.slow
+def test_decode_full_size_sampled_sequences():
+    """The 64 x 256K decode step in the bench's launch configuration; 4 sequences checked."""
+    spec = WORKLOADS["decode_256k_x64"]
+    wl = make_decode(spec, DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode(cfg, wl)
+    for bb in (0, 17, 42, 63):
+        check_decode_seq(cfg, wl, bb, idx, cnt, out, lse)
+
+
+# ----------------------------------------------------------------------------- full-size prefill, sampled rows
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["needle_prefill_32k", "drift_prefill_128k"])
+def test_large_prefill_sampled_rows(name):
+    spec = WORKLOADS[name]
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    gpu = run_prefill(cfg, wl)
+    needle_rows = [i for (_, i, _) in wl["needles"]][:16]
+    rows = QC.sample_rows(spec.n, cfg.k_b, cfg.r, needle_rows, 24, seed=spec.seed)
+    res = QC.oracle_rows(wl, rows, cfg=cfg)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0],
+                            cfg.k_b, cfg.r)
+    assert st["exact"] >= 0.9 * len(rows), st
