@@ -181,6 +181,9 @@ def main():
     ap.add_argument("--impl", choices=["qsa", "reference"], default="qsa")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--prefill-workload", default=PREFILL,
+                    help="prefill workload name (smaller ones serve profiling runs)")
+    ap.add_argument("--decode-workload", default=DECODE, help="decode workload name, or 'none'")
     args = ap.parse_args()
 
     import torch
@@ -189,7 +192,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    pspec, dspec = WORKLOADS[PREFILL], WORKLOADS[DECODE]
+    pspec = WORKLOADS[args.prefill_workload]
+    dspec = WORKLOADS[DECODE if args.decode_workload == "none" else args.decode_workload]
+    do_decode = args.decode_workload != "none"
     pk = peaks()
 
     if args.impl == "reference":
@@ -226,10 +231,14 @@ def main():
     cfg = qsa.Config(r=pspec.r, k_tokens=pspec.k_tokens, rope_dims=pspec.rope_dims, rope_base=pspec.rope_base)
     wl = make_prefill(pspec, dev)
     pre = qsa.QsaPrefill(cfg, 1, pspec.n, pspec.hq, pspec.hkv, device=dev)
-    dwl = make_decode(dspec, dev)
     dcfg = qsa.Config(r=dspec.r, k_tokens=dspec.k_tokens, rope_dims=dspec.rope_dims, rope_base=dspec.rope_base)
-    dec = qsa.QsaDecode(dcfg, dspec.batch, dwl["n_blocks"], dspec.hq, dspec.hkv, device=dev)
-    dq = dwl["q"][:, 0].contiguous()
+    if do_decode:
+        dwl = make_decode(dspec, dev)
+        dec = qsa.QsaDecode(dcfg, dspec.batch, dwl["n_blocks"], dspec.hq, dspec.hkv, device=dev)
+        dq = dwl["q"][:, 0].contiguous()
+    else:
+        dwl = {"cache_len": dspec.cache_len}
+        dec = dq = None
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     names = ["compress", "index_prefill", "attn_prefill", "index_decode", "attn_decode"]
@@ -243,11 +252,15 @@ def main():
         qsa.qsa_sparse_attn_prefill(cfg, wl["q"], wl["k"], wl["v"], pre.q_pos, pre.idx, pre.count,
                                     pre.out, pre.lse)
         evs[3].record(stream)
-        q_pos = dwl["cache_lens"] - 1
-        qsa.qsa_index_topk(dcfg, dwl["q_idx"], dwl["kbar"], q_pos, dwl["n_blocks"], dec.idx, dec.count, dec.ws_idx)
+        if do_decode:
+            q_pos = dwl["cache_lens"] - 1
+            qsa.qsa_index_topk(dcfg, dwl["q_idx"], dwl["kbar"], q_pos, dwl["n_blocks"], dec.idx, dec.count,
+                               dec.ws_idx)
         evs[4].record(stream)
-        qsa.qsa_sparse_attn_decode(dcfg, dq, dwl["k"], dwl["v"], dwl["cache_lens"], dec.idx.view(dspec.batch, -1),
-                                   dec.count.view(dspec.batch), dec.out, dec.ws_attn, dec.lse)
+        if do_decode:
+            qsa.qsa_sparse_attn_decode(dcfg, dq, dwl["k"], dwl["v"], dwl["cache_lens"],
+                                       dec.idx.view(dspec.batch, -1), dec.count.view(dspec.batch), dec.out,
+                                       dec.ws_attn, dec.lse)
         evs[5].record(stream)
 
     mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(6)]
@@ -303,8 +316,10 @@ def main():
                           "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s"},
         "attn_prefill": {"bound": "hbm", "achieved": pw["attn_gather_bytes"] / (mean["attn_prefill"] * 1e-3) / 1e9,
                          "peak": hbm, "unit": "GB/s"},
-        "decode": {"bound": "hbm", "achieved": dwk["bytes"] / (decode_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s"},
     }
+    if do_decode:
+        roofs["decode"] = {"bound": "hbm", "achieved": dwk["bytes"] / (decode_ms * 1e-3) / 1e9, "peak": hbm,
+                           "unit": "GB/s"}
     for v in roofs.values():
         v["frac"] = v["achieved"] / v["peak"]
     dominant = max(["compress", "index_prefill", "attn_prefill"], key=lambda nm: mean[nm])
@@ -319,7 +334,8 @@ def main():
         "decode_us_per_step": decode_ms * 1e3,
         "prefill_ms": prefill_ms,
         "parts_ms": mean,
-        "config": {"workload": f"{PREFILL} + {DECODE}", "prefill_tokens": pspec.n, "prefill_batch": 1,
+        "config": {"workload": f"{pspec.name} + {dspec.name if do_decode else 'no decode'}",
+                   "prefill_tokens": pspec.n, "prefill_batch": 1,
                    "decode_batch": dspec.batch, "decode_ctx": dspec.ctx, "K": pspec.k_tokens, "r": pspec.r,
                    "Hq": pspec.hq, "Hkv": pspec.hkv, "H_idx": pspec.h_idx, "d": pspec.d,
                    "l2": "256 MiB buffer written between steps, outside the timed events",
@@ -328,9 +344,11 @@ def main():
         "gpu_launches": int(launches), "clocks": clk, "wall_s_timed": wall,
     }
 
-    if not args.no_e2e and rank == 0:
+    if not do_decode:
+        line["decode_us_per_step"] = None
+    if not args.no_e2e and rank == 0 and do_decode:
         line["e2e"] = e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev)
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline and rank == 0 and do_decode:
         ot = oracle_timing(pspec, dspec, rows_per_step=3, steps=1)
         line["cpu_baseline"] = {"value": pspec.n / ot["prefill_s"], "unit": "tokens/s", "cores": ot["cores"],
                                 "kind": "oracle", "sample": ot["sample"],
