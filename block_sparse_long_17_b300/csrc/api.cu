@@ -239,3 +239,6 @@ uint64_t qsa_launch_count(void) { return __atomic_load_n(&launch_counter(), __AT
 const char* qsa_version(void) { return "qsa-b300 0.1 sm_103a"; }
 
 }  // extern "C"
+
+// Decode entry point with library-owned static scratch (no allocation).
+#include "decode_noalloc.cu"

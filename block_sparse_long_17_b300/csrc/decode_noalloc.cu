@@ -1,0 +1,86 @@
+// Decode attention for callers that cannot allocate device memory.
+//
+// qsa_sparse_attn_decode needs a caller-provided workspace for its per-split
+// partial results.  Some callers have no way to provide one: code running
+// inside a framework or plugin that owns every device allocation, code paths
+// that must not touch the allocator (no cudaMalloc or pool call allowed), or
+// small C hosts without an allocator of their own.  For them this file holds a
+// second entry point that keeps the partials in a fixed array of static device
+// memory instead.  The paper has no counterpart of this; it is a packaging
+// choice of this library.
+//
+// The array is a file-scope __device__ variable, so every device that loads
+// the library holds kNoAllocScratchBytes of it until the process exits.  Host
+// code cannot use the array's name as a device address (on the host it only
+// names a stand-in object), so the entry point looks up the real address once
+// per device with cudaGetSymbolAddress, with that device current, and hands it
+// to the kernels.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace qsa {
+
+// QSA_NOALLOC_SCRATCH_BYTES (32 MiB): enough for the partials of 64 sequences x
+// 2 kv heads at K = 2048, r = 4 (33 splits of 64 tokens, 4160 B per split and
+// head chunk).
+constexpr size_t kNoAllocScratchBytes = QSA_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+struct NoAllocSlot {
+  std::once_flag once;
+  void* ptr = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+
+NoAllocSlot g_noalloc_slots[kNoAllocMaxDevices];
+
+// Device address of the scratch array on the current device (looked up once).
+cudaError_t noalloc_scratch_ptr(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  NoAllocSlot& s = g_noalloc_slots[dev];
+  std::call_once(s.once, [&s]() {
+    void* p = nullptr;
+    s.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    s.ptr = (s.err == cudaSuccess) ? p : nullptr;
+  });
+  *out = s.ptr;
+  return s.err;
+}
+
+}  // namespace
+}  // namespace qsa
+
+extern "C" qsa_status qsa_sparse_attn_decode_noalloc(const qsa_config* cfg, const void* q,
+                                                     const void* k_cache, const void* v_cache,
+                                                     int64_t L_cap, const int64_t* cache_len,
+                                                     const int32_t* idx, const int32_t* count,
+                                                     int64_t B, int32_t Hq, int32_t Hkv, float scale,
+                                                     void* out, float* lse, qsa_stream_t stream) {
+  using namespace qsa;
+  const size_t need = qsa_sparse_attn_decode_workspace(cfg, B, Hq, Hkv);
+  if (B > 0 && need == 0) {
+    // Invalid arguments: let the regular entry point report which status applies.
+    return qsa_sparse_attn_decode(cfg, q, k_cache, v_cache, L_cap, cache_len, idx, count, B, Hq,
+                                  Hkv, scale, out, lse, nullptr, 0, stream);
+  }
+  if (need > kNoAllocScratchBytes) {
+    std::fprintf(stderr,
+                 "qsa_sparse_attn_decode_noalloc: this batch needs %zu bytes of scratch, above the "
+                 "fixed %zu; use qsa_sparse_attn_decode with a workspace or split the batch\n",
+                 need, kNoAllocScratchBytes);
+    return QSA_ERR_WORKSPACE;
+  }
+  void* scratch = nullptr;
+  cudaError_t e = noalloc_scratch_ptr(&scratch);
+  if (e != cudaSuccess) return from_cuda(e);
+  return qsa_sparse_attn_decode(cfg, q, k_cache, v_cache, L_cap, cache_len, idx, count, B, Hq, Hkv,
+                                scale, out, lse, scratch, kNoAllocScratchBytes, stream);
+}

@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED",
 EXPORTED = [
     "qsa_default_config", "qsa_num_selected_blocks", "qsa_compress_keys",
     "qsa_index_topk_workspace", "qsa_index_topk", "qsa_sparse_attn_prefill",
-    "qsa_sparse_attn_decode_workspace", "qsa_sparse_attn_decode", "qsa_status_string",
+    "qsa_sparse_attn_decode_workspace", "qsa_sparse_attn_decode", "qsa_sparse_attn_decode_noalloc",
+    "qsa_status_string",
     "qsa_read_device_error", "qsa_launch_count", "qsa_version",
 ]
 
@@ -86,6 +87,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qsa_sparse_attn_prefill": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I64, I32, I32, F, P, P, P]),
         "qsa_sparse_attn_decode_workspace": (SZ, [C, I64, I32, I32]),
         "qsa_sparse_attn_decode": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, F, P, P, P, SZ, P]),
+        "qsa_sparse_attn_decode_noalloc": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, F, P, P, P]),
         "qsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "qsa_read_device_error": (ctypes.c_int, [P]),
         "qsa_launch_count": (ctypes.c_uint64, []),
@@ -200,6 +202,30 @@ def qsa_sparse_attn_decode(cfg: Config, q: torch.Tensor, k_cache: torch.Tensor,
         ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), L_cap, _ptr(cache_len), _ptr(idx),
         _ptr(count), B, Hq, Hkv, scale, _ptr(out), _ptr(lse), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20  # QSA_NOALLOC_SCRATCH_BYTES in include/qsa.h
+
+
+def qsa_sparse_attn_decode_noalloc(cfg: Config, q: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, cache_len: torch.Tensor, idx: torch.Tensor,
+                                   count: torch.Tensor, out: torch.Tensor,
+                                   lse: torch.Tensor | None = None, scale: float | None = None,
+                                   stream=None) -> None:
+    """qsa_sparse_attn_decode without a workspace: the library keeps the split
+    partials in its own static device array, for callers that cannot allocate.
+    Calls that may overlap on the GPU share that array and must be ordered."""
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        _bf16(t, nm)
+    _i64(cache_len, "cache_len")
+    B, Hq, d = q.shape
+    Hkv, L_cap = k_cache.shape[1], k_cache.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    c = cfg.c_struct()
+    _check("qsa_sparse_attn_decode_noalloc", load_library().qsa_sparse_attn_decode_noalloc(
+        ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), L_cap, _ptr(cache_len), _ptr(idx),
+        _ptr(count), B, Hq, Hkv, scale, _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def qsa_read_device_error(stream=None) -> int:

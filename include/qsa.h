@@ -174,6 +174,41 @@ qsa_status qsa_sparse_attn_decode(const qsa_config* cfg, const void* q, const vo
                                   int32_t Hkv, float scale, void* out, float* lse, void* ws,
                                   size_t ws_bytes, qsa_stream_t stream);
 
+/*
+ * Size of the static scratch array behind qsa_sparse_attn_decode_noalloc.
+ * Every device that loads the library holds this much device memory for it
+ * until the process exits.
+ */
+#define QSA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * qsa_sparse_attn_decode without a workspace argument, for callers that cannot
+ * allocate device memory: code inside a host framework or plugin that owns
+ * every allocation, paths that must not call cudaMalloc or a pool allocator,
+ * or small C hosts with no allocator of their own.  The paper has no
+ * counterpart of this entry point; it only changes where the partial results
+ * of the split decode live.
+ *   Arguments, results and errors are those of qsa_sparse_attn_decode.
+ *   Scratch: a fixed QSA_NOALLOC_SCRATCH_BYTES array of static device memory
+ *     inside the library (32 MiB: 64 sequences x 2 kv heads at K = 2048,
+ *     r = 4 fit).  A call whose qsa_sparse_attn_decode_workspace() size is
+ *     larger returns QSA_ERR_WORKSPACE and launches nothing.
+ *   No allocation: the call makes no cudaMalloc, cudaFree or other allocating
+ *     call.  Its first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on that device.
+ *   Sharing: every call on a device uses the same array, and nothing in it has
+ *     to start at zero (each call writes every partial it later reads).  Calls
+ *     whose kernels can overlap on the GPU (different streams without ordering
+ *     between them) race on the array and give wrong results; order them.
+ */
+qsa_status qsa_sparse_attn_decode_noalloc(const qsa_config* cfg, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          int64_t L_cap, const int64_t* cache_len,
+                                          const int32_t* idx, const int32_t* count, int64_t B,
+                                          int32_t Hq, int32_t Hkv, float scale, void* out,
+                                          float* lse, qsa_stream_t stream);
+
 /* Human-readable name of a status. */
 const char* qsa_status_string(qsa_status s);
 
