@@ -8,8 +8,9 @@
 
 #include "compress.cu"
 #include "index_scan.cu"
-#include "sparse_attn.cu"
 #include "topk_select.cu"
+#include "index_fused.cu"
+#include "sparse_attn.cu"
 
 namespace qsa {
 namespace {
@@ -58,15 +59,23 @@ qsa_status from_cuda(cudaError_t e) {
 }
 
 struct IndexLayout {
+  bool fused;
   size_t qt_off, s_off, total;
   int64_t s_stride, rows_per_launch;
 };
 
-IndexLayout index_layout(int64_t B, int64_t n_q, int64_t n_blocks_max) {
+// Workspace: rotated queries, then either the per-CTA selection buffers of the
+// fused indexer (prefill) or one launch's worth of score rows (decode scan).
+IndexLayout index_layout(int64_t B, int64_t n_q, int64_t n_blocks_max, int k_b) {
   IndexLayout L{};
   const int64_t rows = B * n_q;
+  L.fused = use_fused_indexer(n_q, k_b);
   L.qt_off = 0;
   L.s_off = align_up((size_t)rows * kIdxHeads * kHeadDim * sizeof(__nv_bfloat16));
+  if (L.fused) {
+    L.total = L.s_off + align_up(fused_layout(B, n_q, n_blocks_max).total);
+    return L;
+  }
   L.s_stride = (n_blocks_max + 3) / 4 * 4;
   if (L.s_stride < 4) L.s_stride = 4;
   int64_t per = kScoreChunkBytes / (L.s_stride * (int64_t)sizeof(float));
@@ -121,7 +130,7 @@ qsa_status qsa_compress_keys(const qsa_config* cfg, const void* k_idx, int64_t k
 
 size_t qsa_index_topk_workspace(const qsa_config* cfg, int64_t B, int64_t n_q, int64_t n_blocks_max) {
   if (check_config(cfg) != QSA_OK || B < 0 || n_q < 0 || n_blocks_max < 0) return 0;
-  return index_layout(B, n_q, n_blocks_max).total;
+  return index_layout(B, n_q, n_blocks_max, k_blocks(cfg)).total;
 }
 
 qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* kbar,
@@ -137,7 +146,7 @@ qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* 
   if (!aligned16(q_idx) || (kbar != nullptr && !aligned16(kbar)) || (kbar_stride_b % 8) != 0)
     return QSA_ERR_INVALID_ARG;
   if (B > 1 && kbar_stride_b < n_blocks_max * kHeadDim) return QSA_ERR_INVALID_ARG;
-  const IndexLayout L = index_layout(B, n_q, n_blocks_max);
+  const IndexLayout L = index_layout(B, n_q, n_blocks_max, k_blocks(cfg));
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return QSA_ERR_INVALID_ARG;
   if (ws_bytes < L.total) return QSA_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -148,6 +157,10 @@ qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* 
   cudaError_t e = launch_rotate_queries(static_cast<const __nv_bfloat16*>(q_idx), q_pos, B, n_q, r,
                                         rope_params(cfg), qt, st);
   if (e != cudaSuccess) return from_cuda(e);
+  if (L.fused) {
+    return from_cuda(launch_index_fused(qt, static_cast<const __nv_bfloat16*>(kbar), kbar_stride_b, q_pos, B,
+                                        n_q, n_blocks_max, r, k_b, idx, count, w + L.s_off, st));
+  }
   const int64_t rows = B * n_q;
   for (int64_t lo = 0; lo < rows; lo += L.rows_per_launch) {
     const int64_t nr = rows - lo < L.rows_per_launch ? rows - lo : L.rows_per_launch;

@@ -1,0 +1,939 @@
+// Fused QSA indexer for prefill: block scores on the tcgen05 tensor cores and an
+// exact top-k_B per query row, without storing the score matrix.
+//
+// "On the Design of Qwen3.8-Next Architecture", research-hub notes, Key ideas,
+// QSA compressed-indexer bullet: I_ib = sum_h ReLU(<q_i^h, kbar_b>) over the 4
+// indexer heads, top k_B = ceil(K / r) blocks per query; paperglide reader,
+// "Qwen Sparse Attention" step 3 (block-causal mask) and step 4 (top-K_B).
+//
+// Layout of the work.  A persistent CTA takes tiles of 64 consecutive query
+// tokens of one sequence.  For a chunk of 128 compressed blocks, 8 tcgen05 MMAs
+// (16 head dims each) compute D[block][token * 4 + head] = <kbar_block,
+// qt_token^head>: M = 128 blocks (A = the kbar chunk, streamed through a 2-stage
+// TMA ring), N = 256 (B = the tile's 64 x 4 rotated query rows, loaded once per
+// tile), fp32 accumulators in TMEM (two buffers of 256 columns).  A TMEM lane is
+// then one block holding the four heads of each token in adjacent columns, so a
+// thread finishes a score with 4 max + 3 add instructions.
+//
+// Exact selection in one pass over the blocks.
+//   1. Pilot: a strided sample of the tile's chunks (about 1/16) is scored
+//      first and binned per token into 512 bins of 1/16 octave of the fp32
+//      score (16-bit counters, two per word).  From it each token takes a
+//      threshold tau above which about 1.5 k_B of its scores are expected.
+//   2. Collect: every chunk is scored; each (token, block) with score >= tau is
+//      appended (bit pattern u, block id) to the token's buffer in global memory.
+//   3. Finalize (4 separate warps, overlapped with the next tile): if the buffer
+//      holds between k_B and kFCap entries it contains the whole top-k_B; a radix
+//      descent on u finds the k_B-th value, equal values go to the lower block
+//      ids, and the winners are sorted by block id.  Rows whose buffer fell
+//      outside that range are queued for the exact fallback kernel (score the
+//      whole row, radix-select it), so the result is always exact.
+//
+// Every wait is a bounded mbarrier wait; on timeout the CTA raises its abort
+// flag, every role leaves its loop, in-flight copies and MMAs are waited for
+// (bounded), TMEM is freed and the device error word reports the timeout.
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace qsa {
+
+constexpr int kTT = 64;                  // query tokens per tile
+constexpr int kNRows = kTT * kIdxHeads;  // 256: MMA N (token, head rows)
+constexpr int kMB = 128;                 // blocks per chunk: MMA M
+constexpr int kAStages = 2;              // kbar TMA ring depth
+constexpr int kEpiWarps = 8;             // 2 per TMEM lane quarter
+constexpr int kFinWarps = 4;
+constexpr int kFThreads = 32 * (2 + kEpiWarps + kFinWarps);  // 448
+constexpr uint32_t kTmemCols = 2 * kNRows;                   // 512: two accumulators
+constexpr int kPBins = 512;              // pilot bins (1/16 octave), packed 2 per word
+constexpr int kPShift = 19;              // bits below the bin index
+constexpr int kPBase = 1904;             // (bits of 2^-8) >> 19
+constexpr int kFinRegs = 48;             // entries per lane in finalize
+constexpr int kFCap = 32 * kFinRegs;     // 1536: most entries a token may collect
+constexpr int kSeg = 512;                // entries per (token, TMEM lane quarter) segment
+constexpr int kFMaxKb = 512;             // largest k_B the fused path handles
+constexpr int kFMaxCtas = 160;           // >= SM count; sizes the buffers
+constexpr int kFMinRows = 64;            // fewer query rows per sequence: scan path
+constexpr int kFbCtas = 148;             // fallback kernel CTAs (one row each at a time)
+constexpr uint32_t kABytes = kMB * 128 * 2;     // 32 KB
+constexpr uint32_t kBBytes = kNRows * 128 * 2;  // 64 KB
+
+// Optional per-role cycle counters for tuning builds (-DQSA_FUSED_PROF).
+#ifdef QSA_FUSED_PROF
+__device__ unsigned long long g_fused_prof[kFMaxCtas][16];
+#define FPROF_T0(name) const long long name = clock64()
+#define FPROF_ADD(slot, t0) atomicAdd(&g_fused_prof[blockIdx.x][slot], (unsigned long long)(clock64() - (t0)))
+#define FPROF_CNT(slot, v) atomicAdd(&g_fused_prof[blockIdx.x][slot], (unsigned long long)(v))
+#else
+#define FPROF_T0(name)
+#define FPROF_ADD(slot, t0)
+#define FPROF_CNT(slot, v)
+#endif
+
+struct FinTile {
+  int64_t bb, tok0, i0;
+  int nvalid;
+};
+
+struct FusedSmem {
+  uint8_t a[kAStages][2][kMB * 128];   // kbar chunk, dims 0-63 | 64-127 (SW128)
+  uint8_t b[2][kNRows * 128];          // rotated queries of the tile, same split
+  uint32_t phist[kTT][kPBins / 2];     // pilot counts, two 16-bit bins per word
+  uint32_t fin_hist[kFinWarps][512];
+  int32_t sortbuf[kFinWarps][kFMaxKb];  // k_B winners before sorting
+  uint32_t tau[kTT];
+  int wcnt[2][4][kTT];                 // entries per (slot, lane quarter, token)
+  FinTile fin[2];
+  int fin_stop[2];
+  uint64_t a_full[kAStages], a_empty[kAStages];
+  uint64_t tfull[2], tempty[2];
+  uint64_t b_full, b_empty, pilot_bar, tau_bar, mma_done;
+  uint64_t fin_full[2], fin_empty[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t kFusedSmemBytes = sizeof(FusedSmem) + 1024;  // + alignment slack
+
+struct TileMeta {
+  int64_t bb, tok0, i0;
+  int nvalid;
+  int nchunks;   // chunks of kMB blocks covering the last row's visible blocks
+  int ngroups;   // complete 16-block groups visible to the last row
+  int mc;        // pilot chunks per phase: ceil(ngroups / kMB)
+  int nphase;    // pilot phases p: blocks 16 m + p are sampled
+  int npilot;    // nphase * mc pilot chunks
+  bool mma;
+};
+
+constexpr int kPilotStride = 16;   // the pilot samples every 16th block (per phase)
+constexpr int kPilotMin = 3072;    // at least this many pilot samples per row when possible
+
+__device__ __forceinline__ TileMeta tile_meta(int64_t t, int64_t tiles_per_seq, int64_t n_q,
+                                              const int64_t* q_pos, int rshift, int k_b, int64_t c_cap) {
+  TileMeta m;
+  m.bb = t / tiles_per_seq;
+  m.tok0 = (t % tiles_per_seq) * kTT;
+  const int64_t rem = n_q - m.tok0;
+  m.nvalid = rem < kTT ? (int)rem : kTT;
+  m.i0 = q_pos[m.bb] + m.tok0;
+  int64_t c = (m.i0 + m.nvalid) >> rshift;
+  if (c > c_cap) c = c_cap;
+  m.mma = c > k_b;
+  m.nchunks = (int)((c + kMB - 1) / kMB);
+  m.ngroups = (int)(c / kPilotStride);
+  m.mc = (m.ngroups + kMB - 1) / kMB;
+  if (m.ngroups == 0) {
+    m.nphase = 0;
+  } else {
+    int np = (kPilotMin + m.ngroups - 1) / m.ngroups;
+    m.nphase = np < 1 ? 1 : (np > kPilotStride ? kPilotStride : np);
+  }
+  m.npilot = m.nphase * m.mc;
+  return m;
+}
+
+__device__ __forceinline__ int64_t token_c(const TileMeta& m, int t, int rshift, int64_t c_cap) {
+  int64_t c = (m.i0 + t + 1) >> rshift;
+  return c > c_cap ? c_cap : c;
+}
+
+// Bounded wait executed by every lane of a warp; the outcome is made uniform so
+// that a warp never splits across a collective (TMEM loads, shuffles).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned sleep_ns = 0) {
+  const bool w = sm100::mbar_wait(bar, parity, abort_flag, sm100::kWaitCycles, sleep_ns);
+  return __all_sync(0xffffffffu, w);
+}
+
+__device__ __forceinline__ int range_shift(uint32_t lo, uint32_t hi) {
+  const int nb = 32 - __clz(hi - lo);
+  return nb > 9 ? nb - 9 : 0;
+}
+
+// One refinement round: `hist` holds the 512-bin histogram of the entries in
+// [lo, hi]; keep the bin where the count from the top reaches `need`.  mode
+// becomes 1 (every entry of the new range wins), 2 (single value: `need` of its
+// entries win) or stays 0.
+__device__ __forceinline__ void refine_round(uint32_t* hist, uint32_t& lo, uint32_t& hi, int& need,
+                                             int& mode, int shift) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  const int base_bin = (31 - lane) * 16;  // lane owns 16 bins, scanned from the top
+  int loc[16], sum = 0;
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    loc[q] = (int)hist[base_bin + 15 - q];
+    sum += loc[q];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int above0 = incl - sum;
+  const bool cross = above0 < need && above0 + sum >= need;
+  const unsigned who = __ballot_sync(0xffffffffu, cross);
+  uint32_t nlo = 0, nhi = 0;
+  int nneed = 0, nmode = 0;
+  if (cross) {
+    int above = above0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      if (above + loc[q] >= need) {
+        const int bin = base_bin + 15 - q;
+        const uint32_t l = lo + ((uint32_t)bin << shift);
+        const uint32_t span = (1u << shift) - 1u;
+        nlo = l;
+        nhi = (hi - l) < span ? hi : l + span;
+        nneed = need - above;
+        nmode = (loc[q] == nneed) ? 1 : (nlo == nhi ? 2 : 0);
+        break;
+      }
+      above += loc[q];
+    }
+  }
+  const int src = who ? __ffs(who) - 1 : 0;
+  lo = __shfl_sync(0xffffffffu, nlo, src);
+  hi = __shfl_sync(0xffffffffu, nhi, src);
+  need = __shfl_sync(0xffffffffu, nneed, src);
+  mode = who ? __shfl_sync(0xffffffffu, nmode, src) : 1;  // cannot happen; stop safely
+  __syncwarp();
+}
+
+// Entry e of a token's buffer: its 4 segments (one per TMEM lane quarter,
+// kSeg entries apart) holding n0, p2 - p1, p3 - p2, ... entries, read as one list.
+__device__ __forceinline__ const uint2* entry_ptr(const uint2* seg, int e, int p1, int p2, int p3) {
+  const int q = (e >= p1) + (e >= p2) + (e >= p3);
+  const int off = e - (q == 0 ? 0 : (q == 1 ? p1 : (q == 2 ? p2 : p3)));
+  return seg + q * kSeg + off;
+}
+
+// Exact top-k_b of a token's buffer (n entries, k_b <= n <= kFCap, any order):
+// the k_b largest patterns, equal patterns going to the lower block ids; the
+// winners are written to out[] sorted by block id.  One warp.  The patterns
+// stay in registers (entry e = lane + 32 j in slot j); block ids are read back
+// from the buffer only for entries that can win.
+__device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int p1, int p2, int p3, int n,
+                                             int k_b, uint32_t* hist, int32_t* sortbuf,
+                                             int32_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  FPROF_T0(f0);
+  uint32_t ru[kFinRegs];
+#pragma unroll
+  for (int j = 0; j < kFinRegs; ++j) {
+    const int e = lane + 32 * j;
+    ru[j] = e < n ? __ldcg(&entry_ptr(seg, e, p1, p2, p3)->x) : 0u;
+  }
+  FPROF_T0(f1);
+  // Start from the buffer's own pattern range, so the first round's bins are
+  // spread over the entries (they all lie within a few octaves of tau).
+  uint32_t lo = 0xffffffffu, hi = 0;
+#pragma unroll
+  for (int j = 0; j < kFinRegs; ++j) {
+    if (lane + 32 * j < n) {
+      lo = min(lo, ru[j]);
+      hi = max(hi, ru[j]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  int need = k_b, mode = (lo == hi) ? 2 : 0;
+  for (int guard = 0; mode == 0 && guard < 6; ++guard) {  // the range shrinks 2^9-fold per round
+    const int shift = range_shift(lo, hi);
+    for (int j = lane; j < 512; j += 32) hist[j] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kFinRegs; ++j)
+      if (lane + 32 * j < n && ru[j] >= lo && ru[j] <= hi) atomicAdd(&hist[(ru[j] - lo) >> shift], 1u);
+    refine_round(hist, lo, hi, need, mode, shift);
+  }
+  if ((threadIdx.x & 127) == 0) FPROF_ADD(4, f1);
+  FPROF_T0(f2);
+  // Ties at a single value: keep the `need` lowest block ids among them.
+  uint32_t tie_cut = 0xffffffffu;  // tied entries with block id < tie_cut win
+  if (mode == 2) {
+    // Rare path (exact ties at the boundary): re-read the entries from memory.
+    int nt = 0;
+    for (int e = lane; e < n; e += 32) nt += (__ldcg(&entry_ptr(seg, e, p1, p2, p3)->x) == lo) ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o);
+    if (nt > need) {
+      // Radix descent on 0x7fffffff - id (ids are distinct), so the largest
+      // keys are the smallest ids.
+      uint32_t blo = 0, bhi = 0x7fffffffu;
+      int bneed = need, bmode = 0;
+      for (int guard = 0; bmode == 0 && guard < 6; ++guard) {
+        const int shift = range_shift(blo, bhi);
+        for (int j = lane; j < 512; j += 32) hist[j] = 0;
+        __syncwarp();
+        for (int e = lane; e < n; e += 32) {
+          const uint2 x = __ldcg(entry_ptr(seg, e, p1, p2, p3));
+          if (x.x == lo) {
+            const uint32_t key = 0x7fffffffu - x.y;
+            if (key >= blo && key <= bhi) atomicAdd(&hist[(key - blo) >> shift], 1u);
+          }
+        }
+        refine_round(hist, blo, bhi, bneed, bmode, shift);
+      }
+      // With distinct keys the descent ends with every key of [blo, bhi]
+      // winning: key >= blo  <=>  id <= 0x7fffffff - blo.
+      tie_cut = 0x7fffffffu - blo + 1u;
+    }
+  }
+  // Compact the k_b winners into sortbuf (any order); block ids are read back in
+  // batches of 16 entries per lane so their loads overlap.
+  int written = 0;
+#pragma unroll
+  for (int j0 = 0; j0 < kFinRegs; j0 += 16) {
+    if (32 * j0 >= n) break;
+    uint32_t ids[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const int e = lane + 32 * (j0 + jj);
+      ids[jj] = e < n ? __ldcg(&entry_ptr(seg, e, p1, p2, p3)->y) : 0u;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const int j = j0 + jj;
+      const int e = lane + 32 * j;
+      bool win = false;
+      if (e < n) {
+        const bool tied = mode == 2 && ru[j] == lo;
+        win = ru[j] > hi || (mode == 1 && ru[j] >= lo) || (tied && ids[jj] < tie_cut);
+      }
+      const unsigned wm = __ballot_sync(0xffffffffu, win);
+      const int pos = written + __popc(wm & ((1u << lane) - 1u));
+      if (win && pos < k_b) sortbuf[pos] = (int32_t)ids[jj];
+      written += __popc(wm);
+    }
+  }
+  __syncwarp();
+  if ((threadIdx.x & 127) == 0) FPROF_ADD(7, f2);
+  FPROF_T0(f3);
+  // Sort the k_b ids ascending: a 512-key bitonic network in registers, lane L
+  // holding keys 16 L .. 16 L + 15 (padding keys sort last).
+  int key[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int i = 16 * lane + q;
+    key[q] = i < k_b ? sortbuf[i] : 0x7fffffff;
+  }
+#pragma unroll
+  for (int size = 2; size <= kFMaxKb; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 16) {
+        const int lx = stride >> 4;  // partner lane distance
+        const bool upper = (lane & lx) != 0;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int i = 16 * lane + q;
+          const bool asc = (i & size) == 0;
+          const int other = __shfl_xor_sync(0xffffffffu, key[q], lx);
+          // lower element keeps the min when ascending
+          const bool keep_min = (asc != upper);
+          key[q] = keep_min ? min(key[q], other) : max(key[q], other);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          if ((q & stride) == 0) {
+            const int i = 16 * lane + q;
+            const bool asc = (i & size) == 0;
+            const int a = key[q], b = key[q + stride];
+            const bool swap = (a > b) == asc;
+            key[q] = swap ? b : a;
+            key[q + stride] = swap ? a : b;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int i = 16 * lane + q;
+    if (i < k_b) out[i] = key[q];
+  }
+  __syncwarp();
+
+}
+
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(kFThreads, 1)
+index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_kp, const int64_t* __restrict__ q_pos,
+                        int64_t n_q, int64_t tiles_per_seq, int64_t n_tiles, int rshift, int k_b,
+                        int64_t c_cap, int32_t* __restrict__ idx,
+                        int32_t* __restrict__ count, uint2* __restrict__ buf, int64_t* __restrict__ fb_rows,
+                        int* __restrict__ fb_count) {
+  using namespace sm100;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* const smem_base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  FusedSmem& S = *reinterpret_cast<FusedSmem*>(smem_base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &S.abort_flag;
+  FPROF_T0(t_kernel);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&S.a_full[s], 1);
+      mbar_init(&S.a_empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&S.tfull[a], 1);
+      mbar_init(&S.tempty[a], kEpiWarps);
+      mbar_init(&S.fin_full[a], kEpiWarps);
+      mbar_init(&S.fin_empty[a], kFinWarps);
+    }
+    mbar_init(&S.b_full, 1);
+    mbar_init(&S.b_empty, 1);
+    mbar_init(&S.pilot_bar, kEpiWarps);
+    mbar_init(&S.tau_bar, kEpiWarps);
+    mbar_init(&S.mma_done, 1);
+    S.abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int j = threadIdx.x; j < kTT * (kPBins / 2); j += kFThreads) (&S.phist[0][0])[j] = 0;
+  for (int j = threadIdx.x; j < 2 * 4 * kTT; j += kFThreads) (&S.wcnt[0][0][0])[j] = 0;
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_kp);
+  }
+  if (warp == 1) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0, b_uses = 0;
+      bool ok = true;
+      for (int64_t k = blockIdx.x; ok && k < n_tiles; k += gridDim.x) {
+        const TileMeta m = tile_meta(n_tiles - 1 - k, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
+        if (!m.mma) continue;
+        if (!mbar_wait(&S.b_empty, (b_uses & 1) ^ 1, abort_flag, kWaitCycles, 128)) { ok = false; break; }
+        ++b_uses;
+        mbar_arrive_expect_tx(&S.b_full, kBBytes);
+        const int qrow = (int)((m.bb * n_q + m.tok0) * kIdxHeads);
+        tma_load_2d(S.b[0], &tm_q, &S.b_full, 0, qrow);
+        tma_load_2d(S.b[1], &tm_q, &S.b_full, 64, qrow);
+        const int total = m.npilot + m.nchunks;
+        for (int x = 0; x < total; ++x, ++it) {
+          const int st = it % kAStages;
+          if (!mbar_wait(&S.a_empty[st], ((it / kAStages) & 1) ^ 1, abort_flag, kWaitCycles, 64)) { ok = false; break; }
+          mbar_arrive_expect_tx(&S.a_full[st], kABytes);
+          if (x < m.npilot) {  // blocks 16 (kMB kc + row) + ph
+            const int ph = x / m.mc, kc = x % m.mc;
+            tma_load_4d(S.a[st][0], &tm_kp, &S.a_full[st], 0, ph, kc * kMB, (int)m.bb);
+            tma_load_4d(S.a[st][1], &tm_kp, &S.a_full[st], 64, ph, kc * kMB, (int)m.bb);
+          } else {
+            const int ch = x - m.npilot;
+            tma_load_3d(S.a[st][0], &tm_k, &S.a_full[st], 0, ch * kMB, (int)m.bb);
+            tma_load_3d(S.a[st][1], &tm_k, &S.a_full[st], 64, ch * kMB, (int)m.bb);
+          }
+        }
+      }
+      if (!ok) {
+        volatile int never = 0;  // wait (bounded) for copies still in flight
+        for (uint32_t j = (it > kAStages ? it - kAStages : 0); j < it; ++j)
+          mbar_wait(&S.a_full[j % kAStages], (j / kAStages) & 1, &never, 100000000LL);
+        if (b_uses > 0) mbar_wait(&S.b_full, (b_uses - 1) & 1, &never, 100000000LL);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kMB, kNRows);
+      uint32_t it = 0, ct = 0, b_uses = 0;
+      bool ok = true;
+      const uint32_t b0 = smem_u32(S.b[0]), b1 = smem_u32(S.b[1]);
+      for (int64_t k = blockIdx.x; ok && k < n_tiles; k += gridDim.x) {
+        const TileMeta m = tile_meta(n_tiles - 1 - k, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
+        if (!m.mma) continue;
+        if (!mbar_wait(&S.b_full, b_uses & 1, abort_flag, kWaitCycles, 64)) { ok = false; break; }
+        ++b_uses;
+        tc_fence_after();
+        const int total = m.npilot + m.nchunks;
+        for (int x = 0; x < total; ++x, ++it, ++ct) {
+          const int st = it % kAStages;
+          const int acc = ct & 1;
+          if (!mbar_wait(&S.a_full[st], (it / kAStages) & 1, abort_flag, kWaitCycles, 32)) { ok = false; break; }
+          FPROF_T0(t2);
+          if (!mbar_wait(&S.tempty[acc], ((ct >> 1) & 1) ^ 1, abort_flag, kWaitCycles, 32)) { ok = false; break; }
+          FPROF_ADD(3, t2);
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(S.a[st][0]), a1 = smem_u32(S.a[st][1]);
+          const uint32_t d = tmem + (uint32_t)(acc * kNRows);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t aoff = (kk < 4 ? a0 : a1) + (uint32_t)((kk & 3) * 32);
+            const uint32_t boff = (kk < 4 ? b0 : b1) + (uint32_t)((kk & 3) * 32);
+            umma_bf16(d, desc_kmajor_sw128(aoff), desc_kmajor_sw128(boff), idesc, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&S.a_empty[st]);
+          umma_commit(&S.tfull[acc]);
+        }
+        if (ok) umma_commit(&S.b_empty);
+      }
+      umma_commit(&S.mma_done);  // every MMA completes before TMEM is released
+      volatile int never = 0;
+      mbar_wait(&S.mma_done, 0, &never, 100000000LL);
+    }
+  } else if (warp < 2 + kEpiWarps) {
+    // ------------------------------------------------------------ score warps
+    const int ew = warp - 2;            // 0..7
+    const int q4 = warp & 3;            // TMEM lane quarter: blocks 32 q4 .. 32 q4 + 31 of a chunk
+    const int half = ew >> 2;           // columns (tokens) 32 half .. 32 half + 31
+    uint32_t ct = 0, tile_n = 0, pilot_n = 0;
+    bool ok = true;
+    for (int64_t k = blockIdx.x; ok && k < n_tiles; k += gridDim.x) {
+      const TileMeta m = tile_meta(n_tiles - 1 - k, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
+      // Rows that keep every visible block (c <= k_B) are written directly by the
+      // warp owning them (tokens 8 ew .. 8 ew + 7).
+      for (int tt = 0; tt < 8; ++tt) {
+        const int t = 8 * ew + tt;
+        if (t >= m.nvalid) break;
+        const int64_t c = token_c(m, t, rshift, c_cap);
+        if (c > k_b) continue;
+        const int64_t grow = m.bb * n_q + m.tok0 + t;
+        int32_t* out = idx + grow * (int64_t)k_b;
+        for (int j = lane; j < k_b; j += 32) out[j] = j < c ? j : -1;
+        if (lane == 0) count[grow] = (int32_t)c;
+      }
+      if (!m.mma) continue;
+      const int slot = tile_n & 1;
+      const uint32_t tcol = (uint32_t)(half * 128);
+      // Token 32 half + j sits at position pos32 + j; tokens j >= tlim are past the end.
+      const int pos32 = (int)(m.i0 + 32 * half);
+      const int cap32 = (int)(c_cap < 0x7fffffff ? c_cap : 0x7fffffff);
+      const int cmin32 = min((pos32 + 1) >> rshift, cap32);  // smallest c of the half
+      const int total = m.npilot + m.nchunks;
+      for (int x = 0; x < total; ++x, ++ct) {
+        const bool pilot = x < m.npilot;
+        if (x == m.npilot) {
+          // ---- pilot done: thresholds for the tokens this warp owns
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.pilot_bar);
+          if (!warp_wait(&S.pilot_bar, pilot_n & 1, abort_flag)) { ok = false; break; }
+          if (lane < 8) {
+            const int t = 8 * ew + lane;
+            uint32_t tau = 0xffffffffu;  // rows that do not select collect nothing
+            if (t < m.nvalid) {
+              const int64_t c = token_c(m, t, rshift, c_cap);
+              if (c > k_b) {
+                int64_t P = 0;
+                for (int w = 0; w < kPBins / 2; ++w) {
+                  const uint32_t v = S.phist[t][w];
+                  P += (v & 0xffffu) + (v >> 16);
+                }
+                int64_t want = (3 * (int64_t)k_b * P + 2 * c - 1) / (2 * c);  // ceil(1.5 k_B P / c)
+                if (want < 1) want = 1;
+                tau = 0;
+                int64_t acc = 0;
+                for (int bin = kPBins - 1; bin >= 0; --bin) {
+                  const uint32_t v = S.phist[t][bin >> 1];
+                  acc += (bin & 1) ? (v >> 16) : (v & 0xffffu);
+                  if (acc >= want) {
+                    tau = bin == 0 ? 0u : (uint32_t)(kPBase + bin) << kPShift;
+                    break;
+                  }
+                }
+              }
+            }
+            S.tau[t] = tau;
+            for (int w = 0; w < kPBins / 2; ++w) S.phist[t][w] = 0;  // ready for the next tile
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.tau_bar);
+          if (!warp_wait(&S.tau_bar, pilot_n & 1, abort_flag)) { ok = false; break; }
+          ++pilot_n;
+          // The finalize warps must be done with this buffer slot.
+          FPROF_T0(tf);
+          if (!warp_wait(&S.fin_empty[slot], ((tile_n >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+          if (ew == 0 && lane == 0) FPROF_ADD(8, tf);
+        }
+        const int acc = ct & 1;
+        FPROF_T0(ts);
+        if (!warp_wait(&S.tfull[acc], (ct >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (ew == 0 && lane == 0) { FPROF_ADD(5, ts); FPROF_CNT(12, 1); }
+        FPROF_T0(tp);
+        tc_fence_after();
+
+        // This lane's block: pilot chunks hold blocks 16 (kMB kc + row) + ph.
+        const int row = 32 * q4 + lane;
+        int bi;            // block id (< 2^31)
+        bool row_ok = true;
+        if (pilot) {
+          const int ph = x / m.mc, kc = x % m.mc;
+          const int grp = kc * kMB + row;
+          bi = grp * kPilotStride + ph;
+          row_ok = grp < m.ngroups;
+        } else {
+          bi = (x - m.npilot) * kMB + row;
+        }
+        // Segment of (token 32 half + j, this warp's lane quarter) in the slot's buffer.
+        uint2* const seg0 = buf + (((int64_t)(blockIdx.x * 2 + slot) * kTT + 32 * half) * 4 + q4) * kSeg;
+        // Every block of this chunk is visible to every token of this warp's half
+        // when the chunk ends below the first token's visible range.
+        const int chunk_last = pilot ? (m.mc * kMB) * kPilotStride : (x - m.npilot + 1) * kMB;
+        const bool chunk_all_visible = chunk_last <= cmin32;
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          uint32_t v[32];
+          FPROF_T0(tl);
+          tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(acc * kNRows) + tcol + (uint32_t)(32 * g), v);
+          tmem_ld_wait();
+          if (ew == 0 && lane == 0) FPROF_ADD(14, tl);
+          FPROF_T0(tb);
+          // Scores of the 8 tokens 32 half + 8 g + kk for this lane's block.
+          uint32_t uu[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const float sc = (fmaxf(__uint_as_float(v[4 * kk]), 0.f) + fmaxf(__uint_as_float(v[4 * kk + 1]), 0.f)) +
+                             (fmaxf(__uint_as_float(v[4 * kk + 2]), 0.f) + fmaxf(__uint_as_float(v[4 * kk + 3]), 0.f));
+            uu[kk] = __float_as_uint(sc) & 0x7fffffffu;
+          }
+          // Which of the 8 tokens see this block.  Tokens that do not select
+          // (past the end, or c <= k_B) are excluded by their threshold; their
+          // pilot counts are never read.
+          uint32_t vis = row_ok ? 0xffu : 0u;
+          if (!chunk_all_visible) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              int c = (pos32 + 8 * g + kk + 1) >> rshift;
+              c = c < cap32 ? c : cap32;
+              if (bi >= c) vis &= ~(1u << kk);
+            }
+          }
+          const int tg = 32 * half + 8 * g;  // first token of the group
+          if (pilot) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              int bin = (int)(uu[kk] >> kPShift) - kPBase;
+              bin = bin < 0 ? 0 : (bin > kPBins - 1 ? kPBins - 1 : bin);
+              if (vis & (1u << kk)) atomicAdd(&S.phist[tg + kk][bin >> 1], (bin & 1) ? 65536u : 1u);
+            }
+          } else {
+            const uint4 ta = *reinterpret_cast<const uint4*>(&S.tau[tg]);
+            const uint4 tc4 = *reinterpret_cast<const uint4*>(&S.tau[tg + 4]);
+            const uint32_t tauv[8] = {ta.x, ta.y, ta.z, ta.w, tc4.x, tc4.y, tc4.z, tc4.w};
+            const int4 ca = *reinterpret_cast<const int4*>(&S.wcnt[slot][q4][tg]);
+            const int4 cb = *reinterpret_cast<const int4*>(&S.wcnt[slot][q4][tg + 4]);
+            const int base[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+            unsigned tmk[8];
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tmk[kk] = __ballot_sync(0xffffffffu, ((vis >> kk) & 1u) && uu[kk] >= tauv[kk]);
+            const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const int pos = base[kk] + __popc(tmk[kk] & lt);
+              if ((tmk[kk] >> lane) & 1u) {
+                if (pos < kSeg) seg0[(int64_t)(8 * g + kk) * 4 * kSeg + pos] = make_uint2(uu[kk], (uint32_t)bi);
+              }
+            }
+            __syncwarp();
+            if (lane == 0) {
+              *reinterpret_cast<int4*>(&S.wcnt[slot][q4][tg]) =
+                  make_int4(ca.x + __popc(tmk[0]), ca.y + __popc(tmk[1]), ca.z + __popc(tmk[2]), ca.w + __popc(tmk[3]));
+              *reinterpret_cast<int4*>(&S.wcnt[slot][q4][tg + 4]) =
+                  make_int4(cb.x + __popc(tmk[4]), cb.y + __popc(tmk[5]), cb.z + __popc(tmk[6]), cb.w + __popc(tmk[7]));
+            }
+          }
+          if (ew == 0 && lane == 0) { FPROF_ADD(pilot ? 1 : 15, tb); FPROF_CNT(pilot ? 0 : 2, 1); }
+        }
+        FPROF_T0(tz);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.tempty[acc]);
+        if (ew == 0 && lane == 0) { FPROF_ADD(6, tp); FPROF_ADD(13, tz); }
+      }
+      if (!ok) break;
+      // ---- hand the tile's buffers to the finalize warps
+      if (ew == 0 && lane == 0) {
+        FinTile ft;
+        ft.bb = m.bb; ft.tok0 = m.tok0; ft.i0 = m.i0; ft.nvalid = m.nvalid;
+        S.fin[slot] = ft;
+        S.fin_stop[slot] = 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.fin_full[slot]);
+      ++tile_n;
+    }
+    // Stop the finalize warps.
+    if (ok) {
+      const int slot = tile_n & 1;
+      if (warp_wait(&S.fin_empty[slot], ((tile_n >> 1) & 1) ^ 1, abort_flag)) {
+        if (ew == 0 && lane == 0) S.fin_stop[slot] = 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.fin_full[slot]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ finalize warps
+    const int fw = warp - 2 - kEpiWarps;
+    uint32_t fc = 0;
+    while (true) {
+      const int slot = fc & 1;
+      FPROF_T0(tq);
+      if (!warp_wait(&S.fin_full[slot], (fc >> 1) & 1, abort_flag, 256)) break;
+      if (fw == 0 && lane == 0) FPROF_ADD(9, tq);
+      if (*(volatile int*)&S.fin_stop[slot]) break;
+      FPROF_T0(tr);
+      const FinTile ft = S.fin[slot];
+      for (int t = fw; t < kTT; t += kFinWarps) {
+        const int n0 = S.wcnt[slot][0][t], n1 = S.wcnt[slot][1][t];
+        const int n2 = S.wcnt[slot][2][t], n3 = S.wcnt[slot][3][t];
+        const int n = n0 + n1 + n2 + n3;
+        const bool seg_ok = n0 <= kSeg && n1 <= kSeg && n2 <= kSeg && n3 <= kSeg;
+        if (t < ft.nvalid) {
+          int64_t c = (ft.i0 + t + 1) >> rshift;
+          if (c > c_cap) c = c_cap;
+          if (c > k_b) {
+            const int64_t grow = ft.bb * n_q + ft.tok0 + t;
+            if (seg_ok && n >= k_b && n <= kFCap) {
+              const uint2* seg = buf + ((int64_t)(blockIdx.x * 2 + slot) * kTT + t) * 4 * kSeg;
+              finalize_row(seg, n0, n0 + n1, n0 + n1 + n2, n, k_b, S.fin_hist[fw], S.sortbuf[fw],
+                           idx + grow * (int64_t)k_b);
+              if (lane == 0) count[grow] = k_b;
+            } else if (lane == 0) {
+              fb_rows[atomicAdd(fb_count, 1)] = grow;  // the exact fallback kernel takes it
+            }
+          }
+        }
+        __syncwarp();
+        if (lane < 4) S.wcnt[slot][lane][t] = 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.fin_empty[slot]);
+      if (fw == 0 && lane == 0) FPROF_ADD(10, tr);
+      ++fc;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) FPROF_ADD(11, t_kernel);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Exact fallback for rows whose threshold missed: one CTA scores the whole row
+// (m16n8k16 MMAs on kbar rows read straight from memory, the 4 heads in the MMA
+// columns) into its scratch row, then runs the CTA radix selection on it.
+__global__ void __launch_bounds__(kSelThreads)
+index_fallback_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16* __restrict__ kbar,
+                      int64_t kbar_stride_b, const int64_t* __restrict__ q_pos, int64_t n_q, int r, int k_b,
+                      int64_t c_cap, const int64_t* __restrict__ fb_rows, const int* __restrict__ fb_count,
+                      float* __restrict__ scratch, int64_t scratch_stride, int32_t* __restrict__ idx,
+                      int32_t* __restrict__ count) {
+  __shared__ SelectSmem sm;
+  const int n_fb = *fb_count;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, t = lane & 3;
+  float* s = scratch + (int64_t)blockIdx.x * scratch_stride;
+  for (int f = blockIdx.x; f < n_fb; f += gridDim.x) {
+    const int64_t row = fb_rows[f];
+    const int64_t bb = row / n_q;
+    int64_t c = (q_pos[bb] + row % n_q + 1) / r;
+    if (c > c_cap) c = c_cap;
+    // B fragment: columns gid < 4 are the 4 heads, the others zero.
+    uint32_t qf[16];
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(qt + (row * kIdxHeads + (gid & 3)) * kHeadDim + 32 * t);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 v = gid < 4 ? src[u] : make_uint4(0, 0, 0, 0);
+        qf[4 * u] = v.x; qf[4 * u + 1] = v.y; qf[4 * u + 2] = v.z; qf[4 * u + 3] = v.w;
+      }
+    }
+    const __nv_bfloat16* kb = kbar + bb * kbar_stride_b;
+    for (int64_t b0 = 16 * warp; b0 < c; b0 += 16 * (kSelThreads / 32)) {
+      const int64_t ra = b0 + gid < c ? b0 + gid : c - 1;
+      const int64_t rb2 = b0 + gid + 8 < c ? b0 + gid + 8 : c - 1;
+      uint32_t ka[16], kx[16];
+      const uint4* pa = reinterpret_cast<const uint4*>(kb + ra * kHeadDim + 32 * t);
+      const uint4* pb = reinterpret_cast<const uint4*>(kb + rb2 * kHeadDim + 32 * t);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 x = pa[u], y = pb[u];
+        ka[4 * u] = x.x; ka[4 * u + 1] = x.y; ka[4 * u + 2] = x.z; ka[4 * u + 3] = x.w;
+        kx[4 * u] = y.x; kx[4 * u + 1] = y.y; kx[4 * u + 2] = y.z; kx[4 * u + 3] = y.w;
+      }
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t a[4] = {ka[2 * ks], kx[2 * ks], ka[2 * ks + 1], kx[2 * ks + 1]};
+        const uint32_t bq[2] = {qf[2 * ks], qf[2 * ks + 1]};
+        mma_bf16_16816(acc, a, bq);
+      }
+      // acc: (block b0+gid, heads 2t, 2t+1), (b0+gid+8, heads 2t, 2t+1); heads >= 4 are zero.
+      float sa = fmaxf(acc[0], 0.f) + fmaxf(acc[1], 0.f);
+      float sb = fmaxf(acc[2], 0.f) + fmaxf(acc[3], 0.f);
+      sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+      sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+      if (t == 0 && b0 + gid < c) s[b0 + gid] = sa;
+      if (t == 0 && b0 + gid + 8 < c) s[b0 + gid + 8] = sb;
+    }
+    __syncthreads();
+    cta_select_row(s, c, k_b, idx + row * (int64_t)k_b, sm);
+    if (threadIdx.x == 0) count[row] = k_b;
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+
+struct FusedLayout {
+  int64_t tiles_per_seq, n_tiles;
+  size_t buf_off, fb_rows_off, fb_count_off, scratch_off, total;
+  int64_t scratch_stride;
+};
+
+// Workspace of the fused path (after the rotated queries): per-CTA token
+// buffers (2 slots x 64 tokens x 4 segments x kSeg entries), the fallback row list and
+// counter, and the fallback kernel's score rows.
+inline FusedLayout fused_layout(int64_t B, int64_t n_q, int64_t n_blocks_max) {
+  auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  FusedLayout L;
+  L.tiles_per_seq = (n_q + kTT - 1) / kTT;
+  L.n_tiles = B * L.tiles_per_seq;
+  L.buf_off = 0;
+  L.fb_rows_off = al(L.buf_off + (size_t)kFMaxCtas * 2 * kTT * 4 * kSeg * sizeof(uint2));
+  L.fb_count_off = al(L.fb_rows_off + (size_t)B * n_q * sizeof(int64_t));
+  L.scratch_off = al(L.fb_count_off + sizeof(int));
+  L.scratch_stride = (n_blocks_max + 63) / 64 * 64;
+  L.total = al(L.scratch_off + (size_t)kFbCtas * L.scratch_stride * sizeof(float));
+  return L;
+}
+
+inline bool use_fused_indexer(int64_t n_q, int k_b) { return n_q >= kFMinRows && k_b <= kFMaxKb; }
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kbar, int64_t kbar_stride_b,
+                               const int64_t* q_pos, int64_t B, int64_t n_q, int64_t n_blocks_max, int r,
+                               int k_b, int32_t* idx, int32_t* count, void* ws, cudaStream_t st) {
+  const FusedLayout L = fused_layout(B, n_q, n_blocks_max);
+  if (L.n_tiles == 0) return cudaSuccess;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  char* w = static_cast<char*>(ws);
+  CUtensorMap tm_q, tm_k;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)(B * n_q * kIdxHeads)};
+    const cuuint64_t strides[1] = {kHeadDim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kNRows};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(qt), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const int64_t nb = n_blocks_max > 0 ? n_blocks_max : 1;
+    int64_t sb = kbar_stride_b;
+    if (B == 1 || sb < nb * kHeadDim) sb = nb * kHeadDim;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)nb, (cuuint64_t)B};
+    const cuuint64_t strides[2] = {kHeadDim * 2, (cuuint64_t)sb * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kMB, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(kbar), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  CUtensorMap tm_kp;
+  {
+    // The same rows viewed as [B][groups][16][128]: a box of 128 groups at one
+    // phase p loads blocks 16 m + p.  Only complete groups are addressable.
+    const int64_t nb = n_blocks_max > 0 ? n_blocks_max : 1;
+    int64_t sb = kbar_stride_b;
+    if (B == 1 || sb < nb * kHeadDim) sb = nb * kHeadDim;
+    const int64_t groups = nb / kPilotStride > 0 ? nb / kPilotStride : 1;
+    const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kPilotStride, (cuuint64_t)groups, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {kHeadDim * 2, (cuuint64_t)kPilotStride * kHeadDim * 2, (cuuint64_t)sb * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kMB, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (encode(&tm_kp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<__nv_bfloat16*>(kbar), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(index_topk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kFusedSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int* fb_count = reinterpret_cast<int*>(w + L.fb_count_off);
+  cudaError_t e = cudaMemsetAsync(fb_count, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  int64_t grid = sms < kFMaxCtas ? sms : kFMaxCtas;
+  if (grid > L.n_tiles) grid = L.n_tiles;
+  int rshift = 0;  // r is a power of two
+  while ((1 << rshift) < r) ++rshift;
+  index_topk_fused_kernel<<<(unsigned)grid, kFThreads, kFusedSmemBytes, st>>>(
+      tm_q, tm_k, tm_kp, q_pos, n_q, L.tiles_per_seq, L.n_tiles, rshift, k_b, n_blocks_max, idx, count,
+      reinterpret_cast<uint2*>(w + L.buf_off), reinterpret_cast<int64_t*>(w + L.fb_rows_off), fb_count);
+  e = count_launch(cudaGetLastError());
+  if (e != cudaSuccess) return e;
+  index_fallback_kernel<<<kFbCtas, kSelThreads, 0, st>>>(
+      qt, kbar, kbar_stride_b, q_pos, n_q, r, k_b, n_blocks_max, reinterpret_cast<int64_t*>(w + L.fb_rows_off),
+      fb_count, reinterpret_cast<float*>(w + L.scratch_off), L.scratch_stride, idx, count);
+  return count_launch(cudaGetLastError());
+}
+
+#ifdef QSA_FUSED_PROF
+extern "C" int qsa_debug_fused_prof(unsigned long long* host, int reset) {
+  if (cudaMemcpyFromSymbol(host, g_fused_prof, sizeof(g_fused_prof)) != cudaSuccess) return 1;
+  if (reset) {
+    static unsigned long long zeros[kFMaxCtas][16] = {};
+    if (cudaMemcpyToSymbol(g_fused_prof, zeros, sizeof(zeros)) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+extern "C" int qsa_debug_fallback_count(const void* ws, int64_t B, int64_t n_q, int64_t n_blocks_max, int* out) {
+  const FusedLayout L = fused_layout(B, n_q, n_blocks_max);
+  return cudaMemcpy(out, static_cast<const char*>(ws) + L.fb_count_off, sizeof(int), cudaMemcpyDeviceToHost) !=
+         cudaSuccess;
+}
+#endif
+
+}  // namespace qsa

@@ -52,44 +52,31 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   return r;
 }
 
-// S: [n_rows][s_stride] fp32 (row j of this launch is global row row_lo + j);
-// idx: [rows][k_b]; count: [rows].
-__global__ void __launch_bounds__(kSelThreads)
-topk_select_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t* __restrict__ q_pos,
-                   int64_t n_q, int64_t row_lo, int r, int k_b, int64_t c_cap,
-                   int32_t* __restrict__ idx, int32_t* __restrict__ count) {
-  __shared__ int hist[kSelBins];
-  __shared__ int warp_sums[32];
-  __shared__ int sh_total;
-  __shared__ uint32_t sh_lo, sh_hi;
-  __shared__ int sh_need, sh_done;
+struct SelectSmem {
+  int hist[kSelBins];
+  int warp_sums[32];
+  int total;
+  uint32_t lo, hi;
+  int need, done;
+};
 
-  const int64_t row = row_lo + blockIdx.x;
-  const int64_t bb = row / n_q;
-  const int64_t pos = q_pos[bb] + row % n_q;
-  int64_t c = (pos + 1) / r;
-  if (c > c_cap) c = c_cap;  // reported by the scan kernel
-  int32_t* out = idx + row * (int64_t)k_b;
-  if (c <= k_b) {
-    for (int j = threadIdx.x; j < k_b; j += kSelThreads) out[j] = j < c ? j : -1;
-    if (threadIdx.x == 0) count[row] = (int32_t)c;
-    return;
-  }
-  const float* s = S + (int64_t)blockIdx.x * s_stride;
-
+// Exact top-k_b of the scores s[0 .. c) (c > k_b) by one CTA of kSelThreads
+// threads: writes the k_b winners to out[] in ascending block order.
+__device__ void cta_select_row(const float* __restrict__ s, int64_t c, int k_b, int32_t* __restrict__ out,
+                               SelectSmem& sm) {
   // done = 1: winners are key > hi plus every key in [lo, hi];
   // done = 2: lo == hi, winners are key > hi plus the first `need` keys == lo.
   uint32_t lo = 0, hi = 0x7fffffffu;
   int need = k_b, done = 0;
-  while (!done) {
+  for (int guard = 0; !done && guard < 6; ++guard) {  // the range shrinks 2^11-fold per round
     const uint32_t width = hi - lo;
     const int nbits = 32 - __clz(width);
     const int shift = nbits > 11 ? nbits - 11 : 0;
-    for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) hist[j] = 0;
+    for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) sm.hist[j] = 0;
     __syncthreads();
     for (int64_t e = threadIdx.x; e < c; e += kSelThreads) {
-      const uint32_t u = score_key(s[e]);
-      if (u >= lo && u <= hi) atomicAdd(&hist[(u - lo) >> shift], 1);
+      const uint32_t u = score_key(__ldcg(s + e));
+      if (u >= lo && u <= hi) atomicAdd(&sm.hist[(u - lo) >> shift], 1);
     }
     __syncthreads();
     // Counts from the top: thread j owns bins [4(T-1-j), 4(T-1-j)+4) so that the
@@ -99,10 +86,10 @@ topk_select_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t*
     int sum = 0;
 #pragma unroll
     for (int q = 0; q < kSelBinsPerThread; ++q) {
-      loc[q] = hist[base_bin + kSelBinsPerThread - 1 - q];  // descending bins
+      loc[q] = sm.hist[base_bin + kSelBinsPerThread - 1 - q];  // descending bins
       sum += loc[q];
     }
-    const int above0 = block_exclusive_scan(sum, warp_sums, &sh_total);
+    const int above0 = block_exclusive_scan(sum, sm.warp_sums, &sm.total);
     if (above0 < need && above0 + sum >= need) {
       int above = above0;
 #pragma unroll
@@ -113,20 +100,20 @@ topk_select_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t*
           const uint32_t span = shift >= 32 ? 0xffffffffu : ((1u << shift) - 1u);
           const uint32_t nhi = (hi - nlo) < span ? hi : nlo + span;
           const int nneed = need - above;
-          sh_lo = nlo;
-          sh_hi = nhi;
-          sh_need = nneed;
-          sh_done = (loc[q] == nneed) ? 1 : (nlo == nhi ? 2 : 0);
+          sm.lo = nlo;
+          sm.hi = nhi;
+          sm.need = nneed;
+          sm.done = (loc[q] == nneed) ? 1 : (nlo == nhi ? 2 : 0);
           break;
         }
         above += loc[q];
       }
     }
     __syncthreads();
-    lo = sh_lo;
-    hi = sh_hi;
-    need = sh_need;
-    done = sh_done;
+    lo = sm.lo;
+    hi = sm.hi;
+    need = sm.need;
+    done = sm.done;
     __syncthreads();
   }
 
@@ -138,14 +125,14 @@ topk_select_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t*
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       if (e + q < c) {
-        const uint32_t u = score_key(s[e + q]);
+        const uint32_t u = score_key(__ldcg(s + e + q));
         if (u > hi || (done == 1 && u >= lo)) win |= 1u << q;
         else if (done == 2 && u == lo) tie |= 1u << q;
       }
     }
     const int n_tie = __popc(tie);
-    const int tie_before = ties_taken + block_exclusive_scan(n_tie, warp_sums, &sh_total);
-    const int tie_total = sh_total;
+    const int tie_before = ties_taken + block_exclusive_scan(n_tie, sm.warp_sums, &sm.total);
+    const int tie_total = sm.total;
     // Ties are taken in block order while the quota lasts.
 #pragma unroll
     for (int q = 0, k = 0; q < 4; ++q) {
@@ -156,8 +143,8 @@ topk_select_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t*
     }
     ties_taken += tie_total;
     const int n_win = __popc(win);
-    const int before = written + block_exclusive_scan(n_win, warp_sums, &sh_total);
-    const int win_total = sh_total;
+    const int before = written + block_exclusive_scan(n_win, sm.warp_sums, &sm.total);
+    const int win_total = sm.total;
 #pragma unroll
     for (int q = 0, k = 0; q < 4; ++q) {
       if (win & (1u << q)) {
@@ -167,6 +154,27 @@ topk_select_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t*
     }
     written += win_total;
   }
+}
+
+// S: [n_rows][s_stride] fp32 (row j of this launch is global row row_lo + j);
+// idx: [rows][k_b]; count: [rows].
+__global__ void __launch_bounds__(kSelThreads)
+topk_select_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t* __restrict__ q_pos,
+                   int64_t n_q, int64_t row_lo, int r, int k_b, int64_t c_cap,
+                   int32_t* __restrict__ idx, int32_t* __restrict__ count) {
+  __shared__ SelectSmem sm;
+  const int64_t row = row_lo + blockIdx.x;
+  const int64_t bb = row / n_q;
+  const int64_t pos = q_pos[bb] + row % n_q;
+  int64_t c = (pos + 1) / r;
+  if (c > c_cap) c = c_cap;  // reported by the scan kernel
+  int32_t* out = idx + row * (int64_t)k_b;
+  if (c <= k_b) {
+    for (int j = threadIdx.x; j < k_b; j += kSelThreads) out[j] = j < c ? j : -1;
+    if (threadIdx.x == 0) count[row] = (int32_t)c;
+    return;
+  }
+  cta_select_row(S + (int64_t)blockIdx.x * s_stride, c, k_b, out, sm);
   if (threadIdx.x == 0) count[row] = k_b;
 }
 
