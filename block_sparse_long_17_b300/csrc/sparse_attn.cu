@@ -8,20 +8,27 @@
 // attention layout is grouped-query: Hq query heads share Hkv key/value heads.
 //
 // Work item = (query token, kv head, chunk of 8 query heads of that group), one
-// warp each.  Per token the 8 heads of a kv group read the same gathered keys,
-// so the warp computes S^T = K_T Q^T with m16n8k16 MMAs (16 gathered tokens x 8
-// heads per tile) and O^T += V_T^T P^T (16 dims x 8 heads per tile), with an
-// fp32 online softmax in between.  The per-token selection gives no reuse across
-// tokens, so gathered rows go straight from L2/HBM into MMA fragments: every lane
-// reads 64 contiguous bytes of each K or V row it needs (head dims visited in a
-// permuted order that is applied to Q and undone for O), and movmatrix
-// transposes the P and V fragments into operand layout.  There is no shared
-// memory staging on the gather path.
+// warp each; warps are persistent and take items in an order that keeps one kv
+// head's K/V hot in L2.  The per-token selection gives no reuse across tokens,
+// so the kernel is bound by gathering 512 B of K and V per selected token and
+// kv head from L2/HBM.  Each warp streams its gathered rows through its own
+// 3-stage cp.async ring in shared memory (16 tokens = 8 KB of K and V per
+// stage, 16-byte chunks XOR-swizzled by row so that ldmatrix reads are free of
+// bank conflicts), so two stages of loads are always in flight while the third
+// is consumed.  Per stage the warp computes S^T = K Q^T with m16n8k16 MMAs
+// (16 tokens x 8 heads; K fragments by ldmatrix), an fp32 online softmax per
+// head, and O^T += V^T P^T (V fragments by ldmatrix.trans, P transposed by
+// movmatrix).
 #include "common.cuh"
 
 namespace qsa {
 
-constexpr int kAttnWarps = 4;
+constexpr int kAWarps = 8;                                   // warps per CTA
+constexpr int kARing = 3;                                    // cp.async stages per warp
+constexpr int kAGroup = 16;                                  // gathered tokens per stage
+constexpr int kAStageBytes = kAGroup * 2 * kHeadDim * 2;     // K and V rows: 8 KB
+constexpr int kAWarpBytes = kARing * kAStageBytes;           // 24 KB
+constexpr int kASmemBytes = kAWarps * kAWarpBytes;           // 192 KB
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnRow {
@@ -45,60 +52,127 @@ __device__ __forceinline__ int64_t slot_token(const AttnRow& a, int r, int slot)
   return a.c * r + (slot - sel_tok);
 }
 
-__device__ __forceinline__ void load_row64(uint32_t dst[16], const __nv_bfloat16* p) {
-  const uint4* q = reinterpret_cast<const uint4*>(p);
+__device__ __forceinline__ AttnRow make_row(int64_t i, int r, const int32_t* sel, int cnt, int k_b) {
+  AttnRow a;
+  a.i = i;
+  a.c = (i + 1) / r;
+  const int64_t cmax = a.c < k_b ? a.c : k_b;
+  if (cnt < 0 || cnt > cmax) {  // count inconsistent with the position: clamp, report
+    flag_device_error(kDevErrBlockId);
+    cnt = cnt < 0 ? 0 : (int)cmax;
+  }
+  a.cnt = cnt;
+  a.sel = sel;
+  a.n_tok = cnt * r + (int)(i + 1 - a.c * r);
+  return a;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t saddr, uint32_t r[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t saddr, uint32_t r[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+
+// Offset of 16-byte chunk `chunk` (0..15) of row `row` in a stage's K or V
+// tile (rows of 256 B; chunk index XORed with row % 8).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return (uint32_t)(row * 256 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Issue the copies of one stage: gathered slots [s0, s0 + 16) (slots past
+// slot_end re-read the last valid slot; their logits are masked).  Each copy
+// instruction moves two whole rows (lanes 0-15: row 2j, lanes 16-31: row 2j+1,
+// 16 bytes per lane), so every request is a full, contiguous 256-byte row.
+__device__ __forceinline__ void issue_stage(uint32_t kst, const AttnRow& a, int r, int s0, int slot_end,
+                                            const __nv_bfloat16* __restrict__ kh,
+                                            const __nv_bfloat16* __restrict__ vh) {
+  const int lane = threadIdx.x & 31;
+  int slot = s0 + (lane & 15);
+  if (slot >= slot_end) slot = slot_end - 1;
+  const int64_t my_tok = slot_token(a, r, slot);  // token of row lane % 16
+  const int chunk = lane & 15, sub = lane >> 4;
+  const uint32_t vst = kst + kAGroup * 256;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    uint4 v = ldg16(q + u);
-    dst[4 * u] = v.x; dst[4 * u + 1] = v.y; dst[4 * u + 2] = v.z; dst[4 * u + 3] = v.w;
+  for (int j = 0; j < kAGroup / 2; ++j) {
+    const int row = 2 * j + sub;
+    const int64_t tok = __shfl_sync(0xffffffffu, my_tok, row);
+    cp_async16(kst + swz(row, chunk), reinterpret_cast<const char*>(kh + tok * kHeadDim) + chunk * 16);
+    cp_async16(vst + swz(row, chunk), reinterpret_cast<const char*>(vh + tok * kHeadDim) + chunk * 16);
   }
 }
 
 // Attention of one token (row `a`) for 8 query heads (qh0 .. qh0+7, only the
-// first n_heads valid) over gathered slots [slot_beg, slot_end).
-// Results per lane: o[mt][e] = unnormalised O^T (dims of m-tile mt, heads 2t,
-// 2t+1), running max m2[2] (log2 units, scale folded in) and sum l[2] of the
-// lane's heads 2t, 2t+1 (already reduced across the warp).
+// first n_heads valid) over gathered slots [slot_beg, slot_end), slot_beg <
+// slot_end.  `ring` is the warp's kARing-stage buffer (shared-window address).
+// Results per lane: o[mt][e] = unnormalised O^T (dims 16 mt + gid (+8), heads
+// 2t, 2t+1), running max m2[2] (log2 units, scale folded in) and sum l[2] of
+// the lane's heads 2t, 2t+1 (reduced across the warp).
 __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q_heads, int n_heads,
                                              const __nv_bfloat16* __restrict__ kh,
                                              const __nv_bfloat16* __restrict__ vh, const AttnRow& a,
                                              int r, int slot_beg, int slot_end, float scale_log2,
-                                             float o[8][4], float m2[2], float l[2]) {
+                                             uint32_t ring, float o[8][4], float m2[2], float l[2]) {
   const int lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
-  uint32_t qf[16];
-  if (gid < n_heads) {
-    load_row64(qf, q_heads + gid * kHeadDim + 32 * t);
-  } else {
+  const int ngroups = (slot_end - slot_beg + kAGroup - 1) / kAGroup;
 #pragma unroll
-    for (int u = 0; u < 16; ++u) qf[u] = 0u;
+  for (int p = 0; p < kARing - 1; ++p) {
+    if (p < ngroups) issue_stage(ring + p * kAStageBytes, a, r, slot_beg + p * kAGroup, slot_end, kh, vh);
+    cp_async_commit();
+  }
+  // B fragments of Q^T: lane holds head gid, dims 16 ks + 2t (+1) and + 8.
+  uint32_t qf[8][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(q_heads + gid * kHeadDim);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qf[ks][0] = gid < n_heads ? __ldg(qrow + 8 * ks + t) : 0u;
+      qf[ks][1] = gid < n_heads ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+    }
   }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float mrun0 = -INFINITY, mrun1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // ldmatrix lane roles: matrix mi = lane / 8, row ri = lane % 8.
+  const int mi = lane >> 3, ri = lane & 7;
+  const int krow = ri + 8 * (mi & 1), kchk = mi >> 1;   // K: rows 0-15, chunk 2 ks + kchk
+  const int vrow = ri + 8 * (mi >> 1), vchk = mi & 1;   // V: tokens 0-15, chunk 2 mt + vchk
 
-  for (int s0 = slot_beg; s0 < slot_end; s0 += 16) {
-    const int sa = s0 + gid, sb = s0 + gid + 8;
-    const bool va_ok = sa < slot_end, vb_ok = sb < slot_end;
-    const int64_t ta = slot_token(a, r, va_ok ? sa : s0);
-    const int64_t tb = slot_token(a, r, vb_ok ? sb : s0);
-    uint32_t ka[16], kb[16], xa[16], xb[16];
-    load_row64(ka, kh + ta * kHeadDim + 32 * t);
-    load_row64(kb, kh + tb * kHeadDim + 32 * t);
-    load_row64(xa, vh + ta * kHeadDim + 32 * t);
-    load_row64(xb, vh + tb * kHeadDim + 32 * t);
+  for (int g = 0; g < ngroups; ++g) {
+    const int gi = g + kARing - 1;
+    if (gi < ngroups) issue_stage(ring + (gi % kARing) * kAStageBytes, a, r, slot_beg + gi * kAGroup, slot_end, kh, vh);
+    cp_async_commit();
+    cp_async_wait<kARing - 1>();
+    __syncwarp();
+    const uint32_t kst = ring + (g % kARing) * kAStageBytes;
+    const uint32_t vst = kst + kAGroup * 256;
+    const int s0 = slot_beg + g * kAGroup;
+    const bool va_ok = s0 + gid < slot_end, vb_ok = s0 + gid + 8 < slot_end;
 
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t af[4] = {ka[2 * ks], kb[2 * ks], ka[2 * ks + 1], kb[2 * ks + 1]};
-      const uint32_t bf[2] = {qf[2 * ks], qf[2 * ks + 1]};
-      mma_bf16_16816(sc, af, bf);
+      uint32_t af[4];
+      ldsm_x4(kst + swz(krow, 2 * ks + kchk), af);
+      mma_bf16_16816(sc, af, qf[ks]);
     }
-    // sc: (slot sa, head 2t), (sa, 2t+1), (sb, 2t), (sb, 2t+1)
-    float x0 = va_ok ? sc[0] * scale_log2 : -INFINITY;
-    float x1 = va_ok ? sc[1] * scale_log2 : -INFINITY;
-    float x2 = vb_ok ? sc[2] * scale_log2 : -INFINITY;
-    float x3 = vb_ok ? sc[3] * scale_log2 : -INFINITY;
+    // sc: (slot s0+gid, head 2t), (s0+gid, 2t+1), (s0+gid+8, 2t), (s0+gid+8, 2t+1)
+    const float x0 = va_ok ? sc[0] * scale_log2 : -INFINITY;
+    const float x1 = va_ok ? sc[1] * scale_log2 : -INFINITY;
+    const float x2 = vb_ok ? sc[2] * scale_log2 : -INFINITY;
+    const float x3 = vb_ok ? sc[3] * scale_log2 : -INFINITY;
     float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -123,11 +197,13 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
     const uint32_t pb[2] = {movmatrix_trans(pack_bf16x2(p0, p1)), movmatrix_trans(pack_bf16x2(p2, p3))};
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      const uint32_t af[4] = {movmatrix_trans(xa[2 * mt]), movmatrix_trans(xa[2 * mt + 1]),
-                              movmatrix_trans(xb[2 * mt]), movmatrix_trans(xb[2 * mt + 1])};
-      mma_bf16_16816(o[mt], af, pb);
+      uint32_t av[4];
+      ldsm_x4_t(vst + swz(vrow, 2 * mt + vchk), av);
+      mma_bf16_16816(o[mt], av, pb);
     }
+    __syncwarp();  // the stage is refilled by the next iteration's issue
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -137,91 +213,82 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
   l[0] = l0; l[1] = l1;
 }
 
-// Physical dim of logical dim 16*mt + 8*half + gid in the O^T fragment.
-__device__ __forceinline__ int o_phys_dim(int mt, int half, int gid) {
-  return 32 * (gid >> 1) + 4 * mt + 2 * half + (gid & 1);
-}
-
-__device__ __forceinline__ AttnRow make_row(int64_t i, int r, const int32_t* sel, int cnt, int k_b) {
-  AttnRow a;
-  a.i = i;
-  a.c = (i + 1) / r;
-  const int64_t cmax = a.c < k_b ? a.c : k_b;
-  if (cnt < 0 || cnt > cmax) {  // count inconsistent with the position: clamp, report
-    flag_device_error(kDevErrBlockId);
-    cnt = cnt < 0 ? 0 : (int)cmax;
+// Writes the warp's O^T fragments (scaled per head) as fp32 [8 heads][128] into
+// the warp's ring (generic pointer), then __syncwarp.
+__device__ __forceinline__ void stage_o(float* st, const float o[8][4], float s0, float s1) {
+  const int lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
+  __syncwarp();
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    st[(2 * t) * kHeadDim + 16 * mt + gid] = o[mt][0] * s0;
+    st[(2 * t + 1) * kHeadDim + 16 * mt + gid] = o[mt][1] * s1;
+    st[(2 * t) * kHeadDim + 16 * mt + 8 + gid] = o[mt][2] * s0;
+    st[(2 * t + 1) * kHeadDim + 16 * mt + 8 + gid] = o[mt][3] * s1;
   }
-  a.cnt = cnt;
-  a.sel = sel;
-  a.n_tok = cnt * r + (int)(i + 1 - a.c * r);
-  return a;
+  __syncwarp();
 }
 
-// Prefill: one warp per (token, kv head, 8-head chunk).  Item order puts the kv
-// head outermost so that concurrently running warps gather from one head's K/V.
-__global__ void __launch_bounds__(kAttnWarps * 32)
+// Prefill: persistent warps over (kv head, token, 8-head chunk) items, kv head
+// outermost so that concurrently running warps gather from one head's K/V.
+__global__ void __launch_bounds__(kAWarps * 32, 1)
 sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                            const __nv_bfloat16* __restrict__ v, int64_t L_cap,
                            const int64_t* __restrict__ q_pos, const int32_t* __restrict__ idx,
                            const int32_t* __restrict__ count, int64_t B, int64_t n_q, int Hq, int Hkv,
                            int r, int k_b, float scale, __nv_bfloat16* __restrict__ out,
                            float* __restrict__ lse) {
-  __shared__ float stage[kAttnWarps][8][kHeadDim + 4];
+  extern __shared__ __align__(128) uint8_t attn_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
+  uint8_t* const wbuf = attn_smem + warp * kAWarpBytes;
+  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(wbuf));
   const int group = Hq / Hkv;
   const int n_hc = (group + 7) / 8;
-  const int64_t item = (int64_t)blockIdx.x * kAttnWarps + warp;
   const int64_t per_head = B * n_q * n_hc;
-  if (item >= per_head * Hkv) return;
-  const int g = (int)(item / per_head);
-  const int64_t rem = item % per_head;
-  const int64_t row = rem / n_hc;
-  const int hc = (int)(rem % n_hc);
-  const int64_t bb = row / n_q;
-  const int64_t i = q_pos[bb] + row % n_q;
-  if (i < 0 || i >= L_cap) {  // token outside the K/V buffers: skip, report
-    if (lane == 0) flag_device_error(kDevErrPosition);
-    return;
-  }
-  const AttnRow a = make_row(i, r, idx + row * (int64_t)k_b, count[row], k_b);
-  const int qh0 = g * group + 8 * hc;
-  const int n_heads = min(8, group - 8 * hc);
-  const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
-  const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
-
-  float o[8][4], m2[2], l[2];
-  attend_slots(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, 0, a.n_tok,
-               scale * kLog2e, o, m2, l);
-  const float inv0 = 1.f / l[0], inv1 = 1.f / l[1];
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int d = o_phys_dim(mt, half, gid);
-      stage[warp][2 * t][d] = o[mt][2 * half] * inv0;
-      stage[warp][2 * t + 1][d] = o[mt][2 * half + 1] * inv1;
+  const int64_t items = per_head * Hkv;
+  const int64_t nwarps = (int64_t)gridDim.x * kAWarps;
+  for (int64_t item = (int64_t)blockIdx.x * kAWarps + warp; item < items; item += nwarps) {
+    const int g = (int)(item / per_head);
+    const int64_t rem = item % per_head;
+    const int64_t row = rem / n_hc;
+    const int hc = (int)(rem % n_hc);
+    const int64_t bb = row / n_q;
+    const int64_t i = q_pos[bb] + row % n_q;
+    if (i < 0 || i >= L_cap) {  // token outside the K/V buffers: skip, report
+      if (lane == 0) flag_device_error(kDevErrPosition);
+      continue;
     }
-  }
-  __syncwarp();
-  // Coalesced bf16 stores: lane writes 4 consecutive dims of each head.
-  for (int h = 0; h < n_heads; ++h) {
-    const float* srow = stage[warp][h];
-    const int d = 4 * lane;
-    const uint2 pk = make_uint2(pack_bf16x2(srow[d], srow[d + 1]), pack_bf16x2(srow[d + 2], srow[d + 3]));
-    *reinterpret_cast<uint2*>(out + ((row * Hq) + qh0 + h) * kHeadDim + d) = pk;
-  }
-  if (lse != nullptr && gid == 0) {
-    // natural-log LSE = (m2 + log2 l) * ln 2
-    if (2 * t < n_heads) lse[row * Hq + qh0 + 2 * t] = (m2[0] + log2f(l[0])) * 0.69314718055994531f;
-    if (2 * t + 1 < n_heads) lse[row * Hq + qh0 + 2 * t + 1] = (m2[1] + log2f(l[1])) * 0.69314718055994531f;
+    const AttnRow a = make_row(i, r, idx + row * (int64_t)k_b, count[row], k_b);
+    const int qh0 = g * group + 8 * hc;
+    const int n_heads = min(8, group - 8 * hc);
+    const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
+    const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
+    float o[8][4], m2[2], l[2];
+    attend_slots(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, 0, a.n_tok, scale * kLog2e, ring, o,
+                 m2, l);
+    float* st = reinterpret_cast<float*>(wbuf);
+    stage_o(st, o, 1.f / l[0], 1.f / l[1]);
+    // Coalesced bf16 stores: lane writes 4 consecutive dims of each head.
+    for (int h = 0; h < n_heads; ++h) {
+      const float* srow = st + h * kHeadDim;
+      const int d = 4 * lane;
+      const uint2 pk = make_uint2(pack_bf16x2(srow[d], srow[d + 1]), pack_bf16x2(srow[d + 2], srow[d + 3]));
+      *reinterpret_cast<uint2*>(out + ((row * Hq) + qh0 + h) * kHeadDim + d) = pk;
+    }
+    if (lse != nullptr && gid == 0) {
+      // natural-log LSE = (m2 + log2 l) * ln 2
+      if (2 * t < n_heads) lse[row * Hq + qh0 + 2 * t] = (m2[0] + log2f(l[0])) * 0.69314718055994531f;
+      if (2 * t + 1 < n_heads) lse[row * Hq + qh0 + 2 * t + 1] = (m2[1] + log2f(l[1])) * 0.69314718055994531f;
+    }
+    __syncwarp();  // the ring is reused by the next item
   }
 }
 
-// Decode partials: one warp per (sequence, kv head, 8-head chunk, split of
-// kDecodeSplit slots).  Writes unnormalised O (fp32) with its max and sum.
+// Decode partials: persistent warps over (sequence, kv head, 8-head chunk,
+// split of kDecodeSplit slots) items.  Writes unnormalised O (fp32) with its
+// running max and sum per head.
 constexpr int kDecodeSplit = 64;
 
-__global__ void __launch_bounds__(kAttnWarps * 32)
+__global__ void __launch_bounds__(kAWarps * 32, 1)
 sparse_attn_decode_partial_kernel(const __nv_bfloat16* __restrict__ q,
                                   const __nv_bfloat16* __restrict__ k,
                                   const __nv_bfloat16* __restrict__ v, int64_t L_cap,
@@ -229,57 +296,53 @@ sparse_attn_decode_partial_kernel(const __nv_bfloat16* __restrict__ q,
                                   const int32_t* __restrict__ idx, const int32_t* __restrict__ count,
                                   int64_t B, int Hq, int Hkv, int r, int k_b, int n_split,
                                   float scale, float* __restrict__ part_o, float* __restrict__ part_ml) {
-  __shared__ float stage[kAttnWarps][8][kHeadDim + 4];
+  extern __shared__ __align__(128) uint8_t attn_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
+  uint8_t* const wbuf = attn_smem + warp * kAWarpBytes;
+  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(wbuf));
   const int group = Hq / Hkv;
   const int n_hc = (group + 7) / 8;
-  const int64_t item = (int64_t)blockIdx.x * kAttnWarps + warp;
-  if (item >= B * Hkv * n_hc * n_split) return;
-  const int split = (int)(item % n_split);
-  const int64_t wi = item / n_split;          // (bb, g, hc)
-  const int hc = (int)(wi % n_hc);
-  const int g = (int)((wi / n_hc) % Hkv);
-  const int64_t bb = wi / (n_hc * Hkv);
-  const int64_t i = cache_len[bb] - 1;
-  float* po = part_o + (wi * n_split + split) * (8 * kHeadDim);
-  float* pml = part_ml + (wi * n_split + split) * 16;
-  if (i < 0 || i >= L_cap) {  // cache length outside [1, L_cap]: empty split, report
-    if (lane == 0 && split == 0) flag_device_error(kDevErrPosition);
-    if (lane < 8) { pml[lane] = -INFINITY; pml[8 + lane] = 0.f; }
-    return;
-  }
-  const AttnRow a = make_row(i, r, idx + bb * (int64_t)k_b, count[bb], k_b);
-  const int qh0 = g * group + 8 * hc;
-  const int n_heads = min(8, group - 8 * hc);
-  const int s_beg = split * kDecodeSplit;
-  const int s_end = min(a.n_tok, s_beg + kDecodeSplit);
-  if (s_beg >= s_end) {
-    // Empty split: contributes nothing.
-    if (lane < 8) { pml[lane] = -INFINITY; pml[8 + lane] = 0.f; }
-    return;
-  }
-  const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
-  const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
-  float o[8][4], m2[2], l[2];
-  attend_slots(q + (bb * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end,
-               scale * kLog2e, o, m2, l);
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int d = o_phys_dim(mt, half, gid);
-      stage[warp][2 * t][d] = o[mt][2 * half];
-      stage[warp][2 * t + 1][d] = o[mt][2 * half + 1];
+  const int64_t items = B * Hkv * n_hc * n_split;
+  const int64_t nwarps = (int64_t)gridDim.x * kAWarps;
+  for (int64_t item = (int64_t)blockIdx.x * kAWarps + warp; item < items; item += nwarps) {
+    const int split = (int)(item % n_split);
+    const int64_t wi = item / n_split;          // (bb, g, hc)
+    const int hc = (int)(wi % n_hc);
+    const int g = (int)((wi / n_hc) % Hkv);
+    const int64_t bb = wi / (n_hc * Hkv);
+    const int64_t i = cache_len[bb] - 1;
+    float* po = part_o + (wi * n_split + split) * (8 * kHeadDim);
+    float* pml = part_ml + (wi * n_split + split) * 16;
+    if (i < 0 || i >= L_cap) {  // cache length outside [1, L_cap]: empty split, report
+      if (lane == 0 && split == 0) flag_device_error(kDevErrPosition);
+      if (lane < 8) { pml[lane] = -INFINITY; pml[8 + lane] = 0.f; }
+      continue;
     }
-  }
-  __syncwarp();
-  for (int h = 0; h < 8; ++h) {
-    const float4 x = *reinterpret_cast<const float4*>(&stage[warp][h][4 * lane]);
-    *reinterpret_cast<float4*>(po + h * kHeadDim + 4 * lane) = x;
-  }
-  if (gid == 0) {
-    pml[2 * t] = m2[0]; pml[2 * t + 1] = m2[1];
-    pml[8 + 2 * t] = l[0]; pml[8 + 2 * t + 1] = l[1];
+    const AttnRow a = make_row(i, r, idx + bb * (int64_t)k_b, count[bb], k_b);
+    const int qh0 = g * group + 8 * hc;
+    const int n_heads = min(8, group - 8 * hc);
+    const int s_beg = split * kDecodeSplit;
+    const int s_end = min(a.n_tok, s_beg + kDecodeSplit);
+    if (s_beg >= s_end) {  // empty split: contributes nothing
+      if (lane < 8) { pml[lane] = -INFINITY; pml[8 + lane] = 0.f; }
+      continue;
+    }
+    const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
+    const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
+    float o[8][4], m2[2], l[2];
+    attend_slots(q + (bb * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end, scale * kLog2e, ring, o,
+                 m2, l);
+    float* st = reinterpret_cast<float*>(wbuf);
+    stage_o(st, o, 1.f, 1.f);
+    for (int h = 0; h < 8; ++h) {
+      const float4 x = *reinterpret_cast<const float4*>(st + h * kHeadDim + 4 * lane);
+      *reinterpret_cast<float4*>(po + h * kHeadDim + 4 * lane) = x;
+    }
+    if (gid == 0) {
+      pml[2 * t] = m2[0]; pml[2 * t + 1] = m2[1];
+      pml[8 + 2 * t] = l[0]; pml[8 + 2 * t + 1] = l[1];
+    }
+    __syncwarp();
   }
 }
 
@@ -329,6 +392,25 @@ size_t decode_workspace_bytes(int64_t B, int Hq, int Hkv, int k_b, int r) {
   return (size_t)units * (8 * kHeadDim + 16) * sizeof(float);
 }
 
+// Grid of a persistent attention kernel (<= one CTA per SM); sets the kernel's
+// dynamic shared memory limit on first use.
+static cudaError_t attn_grid(const void* kernel, int which, int64_t items, int* grid) {
+  static bool attr_done[2] = {false, false};
+  if (!attr_done[which]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kASmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done[which] = true;
+  }
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t need = (items + kAWarps - 1) / kAWarps;
+  *grid = (int)(need < sms ? need : sms);
+  return cudaSuccess;
+}
+
 cudaError_t launch_sparse_attn_prefill(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                        const __nv_bfloat16* v, int64_t L_cap, const int64_t* q_pos,
                                        const int32_t* idx, const int32_t* count, int64_t B,
@@ -337,9 +419,11 @@ cudaError_t launch_sparse_attn_prefill(const __nv_bfloat16* q, const __nv_bfloat
   const int n_hc = (Hq / Hkv + 7) / 8;
   const int64_t items = B * n_q * Hkv * n_hc;
   if (items == 0) return cudaSuccess;
-  const int64_t grid = (items + kAttnWarps - 1) / kAttnWarps;
-  sparse_attn_prefill_kernel<<<(unsigned)grid, kAttnWarps * 32, 0, st>>>(
-      q, k, v, L_cap, q_pos, idx, count, B, n_q, Hq, Hkv, r, k_b, scale, out, lse);
+  int grid = 0;
+  cudaError_t e = attn_grid(reinterpret_cast<const void*>(sparse_attn_prefill_kernel), 0, items, &grid);
+  if (e != cudaSuccess) return e;
+  sparse_attn_prefill_kernel<<<grid, kAWarps * 32, kASmemBytes, st>>>(q, k, v, L_cap, q_pos, idx, count, B, n_q,
+                                                                    Hq, Hkv, r, k_b, scale, out, lse);
   return count_launch(cudaGetLastError());
 }
 
@@ -356,10 +440,12 @@ cudaError_t launch_sparse_attn_decode(const __nv_bfloat16* q, const __nv_bfloat1
   float* part_o = reinterpret_cast<float*>(ws);
   float* part_ml = part_o + units * n_split * 8 * kHeadDim;
   const int64_t items = units * n_split;
-  const int64_t grid = (items + kAttnWarps - 1) / kAttnWarps;
-  sparse_attn_decode_partial_kernel<<<(unsigned)grid, kAttnWarps * 32, 0, st>>>(
+  int grid = 0;
+  cudaError_t e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_partial_kernel), 1, items, &grid);
+  if (e != cudaSuccess) return e;
+  sparse_attn_decode_partial_kernel<<<grid, kAWarps * 32, kASmemBytes, st>>>(
       q, k, v, L_cap, cache_len, idx, count, B, Hq, Hkv, r, k_b, n_split, scale, part_o, part_ml);
-  cudaError_t e = count_launch(cudaGetLastError());
+  e = count_launch(cudaGetLastError());
   if (e != cudaSuccess) return e;
   sparse_attn_decode_combine_kernel<<<(unsigned)units, 256, 0, st>>>(part_o, part_ml, B, Hq, Hkv,
                                                                      n_split, out, lse);
