@@ -286,7 +286,7 @@ sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
 // Decode partials: persistent warps over (sequence, kv head, 8-head chunk,
 // split of kDecodeSplit slots) items.  Writes unnormalised O (fp32) with its
 // running max and sum per head.
-constexpr int kDecodeSplit = 64;
+constexpr int kDecodeSplit = 128;
 
 __global__ void __launch_bounds__(kAWarps * 32, 1)
 sparse_attn_decode_partial_kernel(const __nv_bfloat16* __restrict__ q,
@@ -346,7 +346,10 @@ sparse_attn_decode_partial_kernel(const __nv_bfloat16* __restrict__ q,
   }
 }
 
-// Combine the splits of one (sequence, kv head, head chunk): 8 heads x 128 dims.
+// Combine the splits of one (sequence, kv head, head chunk): 8 heads x 128 dims,
+// one warp per head.  Lanes hold the splits' maxima and sums (32 at a time),
+// so the weights come from warp reductions; the partial rows are then read with
+// independent loads (4 dims per lane).
 __global__ void __launch_bounds__(256)
 sparse_attn_decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                                   int64_t B, int Hq, int Hkv, int n_split,
@@ -364,16 +367,36 @@ sparse_attn_decode_combine_kernel(const float* __restrict__ part_o, const float*
   if (h >= n_heads) return;
   const float* ml = part_ml + wi * n_split * 16;
   float mmax = -INFINITY;
-  for (int s = 0; s < n_split; ++s) mmax = fmaxf(mmax, ml[s * 16 + h]);
+  for (int s0 = 0; s0 < n_split; s0 += 32) {
+    float m = s0 + lane < n_split ? __ldg(ml + (s0 + lane) * 16 + h) : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    mmax = fmaxf(mmax, m);
+  }
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < n_split; ++s) {
-    const float ms = ml[s * 16 + h];
-    if (!(ms > -INFINITY)) continue;
-    const float w = exp2f(ms - mmax);
-    L += w * ml[s * 16 + 8 + h];
-    const float4 x = *reinterpret_cast<const float4*>(part_o + ((wi * n_split + s) * 8 + h) * kHeadDim + 4 * lane);
-    acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
+  for (int s0 = 0; s0 < n_split; s0 += 32) {
+    const int sl = s0 + lane;
+    float w = 0.f, wl = 0.f;
+    if (sl < n_split) {
+      const float ms = __ldg(ml + sl * 16 + h);
+      if (ms > -INFINITY) {
+        w = exp2f(ms - mmax);
+        wl = w * __ldg(ml + sl * 16 + 8 + h);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
+    L += wl;
+    const int nn = min(32, n_split - s0);
+#pragma unroll 4
+    for (int j = 0; j < nn; ++j) {
+      const float wj = __shfl_sync(0xffffffffu, w, j);
+      if (wj != 0.f) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(part_o + ((wi * n_split + s0 + j) * 8 + h) * kHeadDim) + lane);
+        acc.x += wj * x.x; acc.y += wj * x.y; acc.z += wj * x.z; acc.w += wj * x.w;
+      }
+    }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;  // L = 0 only for a rejected cache length
   const uint2 pk = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));

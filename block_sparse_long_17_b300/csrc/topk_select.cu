@@ -74,7 +74,18 @@ __device__ void cta_select_row(const float* __restrict__ s, int64_t c, int k_b, 
     const int shift = nbits > 11 ? nbits - 11 : 0;
     for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) sm.hist[j] = 0;
     __syncthreads();
-    for (int64_t e = threadIdx.x; e < c; e += kSelThreads) {
+    // 16-byte loads (score rows are 16-byte aligned), scalar tail.
+    const int64_t c4 = c & ~int64_t(3);
+#pragma unroll 4
+    for (int64_t e = 4 * (int64_t)threadIdx.x; e < c4; e += 4 * kSelThreads) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(s + e));
+      const uint32_t u0 = score_key(x.x), u1 = score_key(x.y), u2 = score_key(x.z), u3 = score_key(x.w);
+      if (u0 >= lo && u0 <= hi) atomicAdd(&sm.hist[(u0 - lo) >> shift], 1);
+      if (u1 >= lo && u1 <= hi) atomicAdd(&sm.hist[(u1 - lo) >> shift], 1);
+      if (u2 >= lo && u2 <= hi) atomicAdd(&sm.hist[(u2 - lo) >> shift], 1);
+      if (u3 >= lo && u3 <= hi) atomicAdd(&sm.hist[(u3 - lo) >> shift], 1);
+    }
+    for (int64_t e = c4 + threadIdx.x; e < c; e += kSelThreads) {
       const uint32_t u = score_key(__ldcg(s + e));
       if (u >= lo && u <= hi) atomicAdd(&sm.hist[(u - lo) >> shift], 1);
     }
@@ -122,10 +133,13 @@ __device__ void cta_select_row(const float* __restrict__ s, int64_t c, int k_b, 
   for (int64_t e0 = 0; e0 < c; e0 += 4 * kSelThreads) {
     const int64_t e = e0 + 4 * threadIdx.x;
     uint32_t win = 0, tie = 0;
+    float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e + 3 < c) x4 = __ldcg(reinterpret_cast<const float4*>(s + e));
+    const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       if (e + q < c) {
-        const uint32_t u = score_key(__ldcg(s + e + q));
+        const uint32_t u = score_key(e + 3 < c ? xs[q] : __ldcg(s + e + q));
         if (u > hi || (done == 1 && u >= lo)) win |= 1u << q;
         else if (done == 2 && u == lo) tie |= 1u << q;
       }
@@ -184,6 +198,210 @@ cudaError_t launch_topk_select(const float* S, int64_t s_stride, const int64_t* 
   if (n_rows <= 0) return cudaSuccess;
   topk_select_kernel<<<(unsigned)n_rows, kSelThreads, 0, st>>>(S, s_stride, q_pos, n_q, row_lo, r,
                                                                k_b, c_cap, idx, count);
+  return count_launch(cudaGetLastError());
+}
+
+
+// ---------------------------------------------------------------------------------------------
+// Two-pass variant for long rows: one pass for the histogram of the top 11
+// bits, one ordered pass that copies every entry at or above the boundary bin
+// into shared memory (at most kSelCand entries, in block order); the remaining
+// refinement and the emission run on that copy.  Rows whose boundary bin is
+// too full fall back to cta_select_row.
+constexpr int kSelCand = 4096;
+
+struct SelectFastSmem {
+  SelectSmem base;
+  uint32_t cu[kSelCand];
+  int32_t cb[kSelCand];
+};
+
+__device__ void cta_select_row_fast(const float* __restrict__ s, int64_t c, int k_b, int32_t* __restrict__ out,
+                                    SelectFastSmem& sm) {
+  // Pass 1: bins of the top 11 bits of the pattern.
+  for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) sm.base.hist[j] = 0;
+  __syncthreads();
+  const int64_t c4 = c & ~int64_t(3);
+#pragma unroll 4
+  for (int64_t e = 4 * (int64_t)threadIdx.x; e < c4; e += 4 * kSelThreads) {
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(s + e));
+    atomicAdd(&sm.base.hist[score_key(x.x) >> 20], 1);
+    atomicAdd(&sm.base.hist[score_key(x.y) >> 20], 1);
+    atomicAdd(&sm.base.hist[score_key(x.z) >> 20], 1);
+    atomicAdd(&sm.base.hist[score_key(x.w) >> 20], 1);
+  }
+  for (int64_t e = c4 + threadIdx.x; e < c; e += kSelThreads) atomicAdd(&sm.base.hist[score_key(__ldcg(s + e)) >> 20], 1);
+  __syncthreads();
+  const int base_bin = (kSelThreads - 1 - threadIdx.x) * kSelBinsPerThread;
+  int loc[kSelBinsPerThread];
+  int sum = 0;
+#pragma unroll
+  for (int q = 0; q < kSelBinsPerThread; ++q) {
+    loc[q] = sm.base.hist[base_bin + kSelBinsPerThread - 1 - q];
+    sum += loc[q];
+  }
+  const int above0 = block_exclusive_scan(sum, sm.base.warp_sums, &sm.base.total);
+  if (above0 < k_b && above0 + sum >= k_b) {
+    int above = above0;
+#pragma unroll
+    for (int q = 0; q < kSelBinsPerThread; ++q) {
+      if (above + loc[q] >= k_b) {
+        const int bin = base_bin + kSelBinsPerThread - 1 - q;
+        sm.base.lo = (uint32_t)bin << 20;
+        sm.base.hi = ((uint32_t)bin << 20) | 0xfffffu;
+        sm.base.need = k_b - above;
+        sm.base.done = above + loc[q];  // entries at or above the bin
+        break;
+      }
+      above += loc[q];
+    }
+  }
+  __syncthreads();
+  uint32_t lo = sm.base.lo, hi = sm.base.hi;
+  int need = sm.base.need;
+  const int ncand = sm.base.done;
+  __syncthreads();
+  if (ncand > kSelCand) {  // boundary bin too full for the copy: general path
+    cta_select_row(s, c, k_b, out, sm.base);
+    return;
+  }
+  // Pass 2: ordered copy of the entries with pattern >= lo.
+  int written = 0;
+  for (int64_t e0 = 0; e0 < c; e0 += 4 * kSelThreads) {
+    const int64_t e = e0 + 4 * threadIdx.x;
+    float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (e + 3 < c) x4 = __ldcg(reinterpret_cast<const float4*>(s + e));
+    const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
+    uint32_t uk[4], take = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uk[q] = 0;
+      if (e + q < c) {
+        uk[q] = score_key(e + 3 < c ? xs[q] : __ldcg(s + e + q));
+        if (uk[q] >= lo) take |= 1u << q;
+      }
+    }
+    const int before = written + block_exclusive_scan(__popc(take), sm.base.warp_sums, &sm.base.total);
+    const int tot = sm.base.total;
+#pragma unroll
+    for (int q = 0, k = 0; q < 4; ++q) {
+      if (take & (1u << q)) {
+        if (before + k < kSelCand) {
+          sm.cu[before + k] = uk[q];
+          sm.cb[before + k] = (int32_t)(e + q);
+        }
+        ++k;
+      }
+    }
+    written += tot;
+  }
+  __syncthreads();
+  // Refine [lo, hi] on the copy (entries > hi are all winners).
+  int done = 0;
+  for (int guard = 0; !done && guard < 6; ++guard) {
+    const uint32_t width = hi - lo;
+    const int nbits = 32 - __clz(width);
+    const int shift = nbits > 11 ? nbits - 11 : 0;
+    for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) sm.base.hist[j] = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < ncand; e += kSelThreads) {
+      const uint32_t u = sm.cu[e];
+      if (u >= lo && u <= hi) atomicAdd(&sm.base.hist[(u - lo) >> shift], 1);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kSelBinsPerThread; ++q) loc[q] = sm.base.hist[base_bin + kSelBinsPerThread - 1 - q];
+    sum = loc[0] + loc[1] + loc[2] + loc[3];
+    const int ab0 = block_exclusive_scan(sum, sm.base.warp_sums, &sm.base.total);
+    if (ab0 < need && ab0 + sum >= need) {
+      int above = ab0;
+#pragma unroll
+      for (int q = 0; q < kSelBinsPerThread; ++q) {
+        if (above + loc[q] >= need) {
+          const int bin = base_bin + kSelBinsPerThread - 1 - q;
+          const uint32_t nlo = lo + ((uint32_t)bin << shift);
+          const uint32_t span = (1u << shift) - 1u;
+          const uint32_t nhi = (hi - nlo) < span ? hi : nlo + span;
+          const int nneed = need - above;
+          sm.base.lo = nlo;
+          sm.base.hi = nhi;
+          sm.base.need = nneed;
+          sm.base.done = (loc[q] == nneed) ? 1 : (nlo == nhi ? 2 : 0);
+          break;
+        }
+        above += loc[q];
+      }
+    }
+    __syncthreads();
+    lo = sm.base.lo;
+    hi = sm.base.hi;
+    need = sm.base.need;
+    done = sm.base.done;
+    __syncthreads();
+  }
+  // Ordered emission from the copy (already in block order).
+  int wr = 0, ties_taken = 0;
+  for (int e0 = 0; e0 < ncand; e0 += 4 * kSelThreads) {
+    const int e = e0 + 4 * threadIdx.x;
+    uint32_t win = 0, tie = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (e + q < ncand) {
+        const uint32_t u = sm.cu[e + q];
+        if (u > hi || (done == 1 && u >= lo)) win |= 1u << q;
+        else if (done == 2 && u == lo) tie |= 1u << q;
+      }
+    }
+    const int tie_before = ties_taken + block_exclusive_scan(__popc(tie), sm.base.warp_sums, &sm.base.total);
+    const int tie_total = sm.base.total;
+#pragma unroll
+    for (int q = 0, k = 0; q < 4; ++q) {
+      if (tie & (1u << q)) {
+        if (tie_before + k < need) win |= 1u << q;
+        ++k;
+      }
+    }
+    ties_taken += tie_total;
+    const int before = wr + block_exclusive_scan(__popc(win), sm.base.warp_sums, &sm.base.total);
+    const int wtot = sm.base.total;
+#pragma unroll
+    for (int q = 0, k = 0; q < 4; ++q) {
+      if (win & (1u << q)) {
+        if (before + k < k_b) out[before + k] = sm.cb[e + q];
+        ++k;
+      }
+    }
+    wr += wtot;
+  }
+}
+
+// One CTA per row; rows with c <= k_b keep every block.
+__global__ void __launch_bounds__(kSelThreads)
+topk_select_fast_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t* __restrict__ q_pos,
+                        int64_t n_q, int64_t row_lo, int r, int k_b, int64_t c_cap,
+                        int32_t* __restrict__ idx, int32_t* __restrict__ count) {
+  __shared__ SelectFastSmem sm;
+  const int64_t row = row_lo + blockIdx.x;
+  const int64_t bb = row / n_q;
+  const int64_t pos = q_pos[bb] + row % n_q;
+  int64_t c = (pos + 1) / r;
+  if (c > c_cap) c = c_cap;
+  int32_t* out = idx + row * (int64_t)k_b;
+  if (c <= k_b) {
+    for (int j = threadIdx.x; j < k_b; j += kSelThreads) out[j] = j < c ? j : -1;
+    if (threadIdx.x == 0) count[row] = (int32_t)c;
+    return;
+  }
+  cta_select_row_fast(S + (int64_t)blockIdx.x * s_stride, c, k_b, out, sm);
+  if (threadIdx.x == 0) count[row] = k_b;
+}
+
+cudaError_t launch_topk_select_fast(const float* S, int64_t s_stride, const int64_t* q_pos, int64_t n_q,
+                                    int64_t row_lo, int64_t n_rows, int r, int k_b, int64_t c_cap, int32_t* idx,
+                                    int32_t* count, cudaStream_t st) {
+  if (n_rows <= 0) return cudaSuccess;
+  topk_select_fast_kernel<<<(unsigned)n_rows, kSelThreads, 0, st>>>(S, s_stride, q_pos, n_q, row_lo, r, k_b, c_cap,
+                                                                    idx, count);
   return count_launch(cudaGetLastError());
 }
 
