@@ -128,6 +128,17 @@ def bus_id_of(dev) -> str | None:
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
+def blas_threads() -> int:
+    """Threads numpy's BLAS uses (the oracle's only multi-threaded part)."""
+    try:
+        from threadpoolctl import threadpool_info
+        return max([p.get("num_threads", 1) for p in threadpool_info()] + [1])
+    except ImportError:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(var, "").isdigit():
+                return int(os.environ[var])
+        return os.cpu_count() or 1
+
 def oracle_timing(pre_spec, dec_spec, rows_per_step: int, steps: int, seed: int = 0) -> dict:
     """Times the CPU oracle, as it stands, on a bounded sample of both workloads.
 
@@ -136,8 +147,6 @@ def oracle_timing(pre_spec, dec_spec, rows_per_step: int, steps: int, seed: int 
     all n rows by the mean row cost.  Decode: one sequence's step, times the batch.
     """
     import numpy as np
-    import torch
-    from threadpoolctl import threadpool_info
 
     from block_sparse_long_17_b300.workloads import make_decode, make_prefill
     from oracle import qsa_oracle as O
@@ -163,7 +172,7 @@ def oracle_timing(pre_spec, dec_spec, rows_per_step: int, steps: int, seed: int 
                       dw["kbar"][0].float().numpy(), dw["k"][0].float().numpy(), dw["v"][0].float().numpy(),
                       dw["cache_len"], r=dec_spec.r, k_tokens=dec_spec.k_tokens)
         dec_times.append((time.perf_counter() - t3) * dec_spec.batch)
-    threads = max([p.get("num_threads", 1) for p in threadpool_info()] + [1])
+    threads = blas_threads()
     return {"prefill_s": statistics.mean(pre_times), "decode_s": statistics.mean(dec_times),
             "cores": threads,
             "sample": (f"per step: compress all {n // r} blocks + {rows_per_step} of {n} prefill rows "

@@ -89,6 +89,9 @@ WORKLOADS = {
     "drift_prefill_128k": PrefillSpec("drift_prefill_128k", n=131072, k_tokens=2048, seed=2, drift=True),
     "decode_256k_x64": DecodeSpec("decode_256k_x64", batch=64, ctx=262144, k_tokens=2048, seed=3),
     "needle_prefill_1m": PrefillSpec("needle_prefill_1m", n=1048576, k_tokens=2048, seed=4, needles=256),
+    # A smaller decode step of the same shape family (a few GB on the device),
+    # for profiling captures.
+    "decode_64k_x64": DecodeSpec("decode_64k_x64", batch=64, ctx=65536, k_tokens=2048, seed=5),
 }
 
 
