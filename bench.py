@@ -331,6 +331,15 @@ def main():
                            "unit": "GB/s"}
     for v in roofs.values():
         v["frac"] = v["achieved"] / v["peak"]
+    # The bound of prefill attention: gathering random 256-byte rows from a buffer
+    # the size of one kv head's K/V (resident in L2), measured on this GPU.
+    kv_bytes = 2 * pspec.n * pspec.d * 2
+    probe_buf = torch.empty((max(kv_bytes, 1 << 20) + 256,), dtype=torch.uint8, device=dev)
+    probe_buf.fill_(1)
+    l2_gather = qsa.qsa_probe_l2_gather(probe_buf)
+    del probe_buf
+    roofs["attn_prefill"]["l2_gather_peak"] = l2_gather
+    roofs["attn_prefill"]["frac_of_l2_gather"] = roofs["attn_prefill"]["achieved"] / l2_gather
     dominant = max(["compress", "index_prefill", "attn_prefill"], key=lambda nm: mean[nm])
     roof = dict(roofs[dominant])
     roof["kernel"] = dominant

@@ -261,3 +261,6 @@ const char* qsa_version(void) { return "qsa-b300 0.1 sm_103a"; }
 
 // Decode entry point with library-owned static scratch (no allocation).
 #include "decode_noalloc.cu"
+
+// Measurement helper for the attention roofline.
+#include "probe.cu"

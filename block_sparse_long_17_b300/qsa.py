@@ -27,7 +27,7 @@ EXPORTED = [
     "qsa_default_config", "qsa_num_selected_blocks", "qsa_compress_keys",
     "qsa_index_topk_workspace", "qsa_index_topk", "qsa_sparse_attn_prefill",
     "qsa_sparse_attn_decode_workspace", "qsa_sparse_attn_decode", "qsa_sparse_attn_decode_noalloc",
-    "qsa_status_string",
+    "qsa_probe_l2_gather", "qsa_status_string",
     "qsa_read_device_error", "qsa_launch_count", "qsa_version",
 ]
 
@@ -88,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qsa_sparse_attn_decode_workspace": (SZ, [C, I64, I32, I32]),
         "qsa_sparse_attn_decode": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, F, P, P, P, SZ, P]),
         "qsa_sparse_attn_decode_noalloc": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, F, P, P, P]),
+        "qsa_probe_l2_gather": (ctypes.c_int, [P, SZ, ctypes.POINTER(ctypes.c_float), P]),
         "qsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "qsa_read_device_error": (ctypes.c_int, [P]),
         "qsa_launch_count": (ctypes.c_uint64, []),
@@ -226,6 +227,14 @@ def qsa_sparse_attn_decode_noalloc(cfg: Config, q: torch.Tensor, k_cache: torch.
     _check("qsa_sparse_attn_decode_noalloc", load_library().qsa_sparse_attn_decode_noalloc(
         ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), L_cap, _ptr(cache_len), _ptr(idx),
         _ptr(count), B, Hq, Hkv, scale, _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def qsa_probe_l2_gather(buf: torch.Tensor, stream=None) -> float:
+    """GB/s of pseudo-random 256-byte row gathers from `buf` (a device tensor)."""
+    out = ctypes.c_float(0.0)
+    _check("qsa_probe_l2_gather", load_library().qsa_probe_l2_gather(
+        _ptr(buf), buf.numel() * buf.element_size(), ctypes.byref(out), _stream(stream)))
+    return float(out.value)
 
 
 def qsa_read_device_error(stream=None) -> int:

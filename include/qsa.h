@@ -209,6 +209,17 @@ qsa_status qsa_sparse_attn_decode_noalloc(const qsa_config* cfg, const void* q,
                                           int32_t Hq, int32_t Hkv, float scale, void* out,
                                           float* lse, qsa_stream_t stream);
 
+/*
+ * Measurement helper (not part of the method): the bandwidth at which the SMs
+ * gather pseudo-random 256-byte rows from `buf` (`bytes` long, 256-byte
+ * aligned, at least 1 MiB; contents are read, not modified, except its last
+ * 256 bytes).  Sparse core attention gathers one 256-byte K row and one V row
+ * per selected token, so with a buffer the size of one kv head's K/V (which
+ * stays in L2) this is the bound of qsa_sparse_attn_prefill.  Synchronises
+ * `stream`; writes GB/s to *gbs.  Allocates nothing.
+ */
+qsa_status qsa_probe_l2_gather(void* buf, size_t bytes, float* gbs, qsa_stream_t stream);
+
 /* Human-readable name of a status. */
 const char* qsa_status_string(qsa_status s);
 
