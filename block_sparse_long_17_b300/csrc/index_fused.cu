@@ -7,27 +7,39 @@
 // "Qwen Sparse Attention" step 3 (block-causal mask) and step 4 (top-K_B).
 //
 // Layout of the work.  A persistent CTA takes tiles of 64 consecutive query
-// tokens of one sequence.  For a chunk of 128 compressed blocks, 8 tcgen05 MMAs
-// (16 head dims each) compute D[block][token * 4 + head] = <kbar_block,
-// qt_token^head>: M = 128 blocks (A = the kbar chunk, streamed through a 2-stage
+// tokens of one sequence.  A chunk is 128 compressed blocks: 8 tcgen05 MMAs
+// (16 head dims each) compute D[row][token * 4 + head] = <kbar_block(row),
+// qt_token^head>: M = 128 rows (A = the kbar chunk, streamed through a 2-stage
 // TMA ring), N = 256 (B = the tile's 64 x 4 rotated query rows, loaded once per
-// tile), fp32 accumulators in TMEM (two buffers of 256 columns).  A TMEM lane is
-// then one block holding the four heads of each token in adjacent columns, so a
-// thread finishes a score with 4 max + 3 add instructions.
+// tile), fp32 accumulators in TMEM (two buffers of 256 columns).  The tile's
+// visible blocks are split into 4 consecutive regions of R = 32 x nchunks
+// blocks; rows 32 q .. 32 q + 31 of chunk x hold blocks q R + 32 x .. + 31, so
+// TMEM lane quarter q walks region q in order.  A TMEM lane holds the four
+// heads of each token in adjacent columns: a thread finishes a score with 7
+// adds (x + |x| is 2 ReLU(x)).
 //
 // Exact selection in one pass over the blocks.
-//   1. Pilot: a strided sample of the tile's chunks (about 1/16) is scored
-//      first and binned per token into 512 bins of 1/16 octave of the fp32
-//      score (16-bit counters, two per word).  From it each token takes a
-//      threshold tau above which about 1.5 k_B of its scores are expected.
+//   1. Pilot: a strided sample of the tile's blocks (every 16th block, in one
+//      or more phases) is scored first and binned per token into 512 bins of
+//      1/16 octave of the fp32 score (16-bit counters, two per word).  From it
+//      each token takes a threshold tau above which about 1.5 k_B of its scores
+//      are expected.
 //   2. Collect: every chunk is scored; each (token, block) with score >= tau is
-//      appended (bit pattern u, block id) to the token's buffer in global memory.
-//   3. Finalize (4 separate warps, overlapped with the next tile): if the buffer
-//      holds between k_B and kFCap entries it contains the whole top-k_B; a radix
+//      appended (bit pattern u of 2 x score, block id) to the token's buffer in
+//      global memory: one segment per TMEM lane quarter, so that no two warps
+//      share a counter.  Segment q lists region q in ascending block order, so
+//      the 4 segments read in turn are in block order.  Counts are stored when
+//      the tile is done.
+//   3. Finalize (a separate kernel, one warp per row): if the buffer holds
+//      between k_B and kFCap entries it contains the whole top-k_B; a radix
 //      descent on u finds the k_B-th value, equal values go to the lower block
-//      ids, and the winners are sorted by block id.  Rows whose buffer fell
-//      outside that range are queued for the exact fallback kernel (score the
-//      whole row, radix-select it), so the result is always exact.
+//      ids, and the winners, compacted in entry order, come out sorted by block
+//      id.  Rows whose buffer fell outside that range are queued for the exact
+//      fallback kernel (score the whole row, radix-select it), so the result is
+//      always exact.
+// Sixteen score warps (four per TMEM lane quarter, 16 tokens each) read the
+// accumulators; the host launches the kernel over ranges of at most
+// kTilesPerLaunch tiles so that the entry buffers stay bounded.
 //
 // Every wait is a bounded mbarrier wait; on timeout the CTA raises its abort
 // flag, every role leaves its loop, in-flight copies and MMAs are waited for
@@ -43,20 +55,22 @@ constexpr int kTT = 64;                  // query tokens per tile
 constexpr int kNRows = kTT * kIdxHeads;  // 256: MMA N (token, head rows)
 constexpr int kMB = 128;                 // blocks per chunk: MMA M
 constexpr int kAStages = 2;              // kbar TMA ring depth
-constexpr int kEpiWarps = 8;             // 2 per TMEM lane quarter
-constexpr int kFinWarps = 4;
-constexpr int kFThreads = 32 * (2 + kEpiWarps + kFinWarps);  // 448
+constexpr int kEpiWarps = 16;            // 4 per TMEM lane quarter
+constexpr int kFThreads = 32 * (2 + kEpiWarps);              // 576
 constexpr uint32_t kTmemCols = 2 * kNRows;                   // 512: two accumulators
 constexpr int kPBins = 512;              // pilot bins (1/16 octave), packed 2 per word
 constexpr int kPShift = 19;              // bits below the bin index
-constexpr int kPBase = 1904;             // (bits of 2^-8) >> 19
+constexpr int kPBase = 1920;             // (bits of 2^-7) >> 19: bins of 2 x score start at 2^-7
 constexpr int kFinRegs = 48;             // entries per lane in finalize
 constexpr int kFCap = 32 * kFinRegs;     // 1536: most entries a token may collect
-constexpr int kSeg = 512;                // entries per (token, TMEM lane quarter) segment
+constexpr int kSeg = kFCap;              // entries per (token, TMEM lane quarter) segment: a
+                                         // quarter may hold all of a row's entries
 constexpr int kFMaxKb = 512;             // largest k_B the fused path handles
 constexpr int kFMaxCtas = 160;           // >= SM count; sizes the buffers
 constexpr int kFMinRows = 64;            // fewer query rows per sequence: scan path
 constexpr int kFbCtas = 148;             // fallback kernel CTAs (one row each at a time)
+constexpr int kTilesPerLaunch = 1024;    // tiles per fused launch (bounds the row buffers: 3 GiB)
+constexpr int kFinKWarps = 4;            // warps per CTA of the finalize kernel
 constexpr uint32_t kABytes = kMB * 128 * 2;     // 32 KB
 constexpr uint32_t kBBytes = kNRows * 128 * 2;  // 64 KB
 
@@ -66,31 +80,24 @@ __device__ unsigned long long g_fused_prof[kFMaxCtas][16];
 #define FPROF_T0(name) const long long name = clock64()
 #define FPROF_ADD(slot, t0) atomicAdd(&g_fused_prof[blockIdx.x][slot], (unsigned long long)(clock64() - (t0)))
 #define FPROF_CNT(slot, v) atomicAdd(&g_fused_prof[blockIdx.x][slot], (unsigned long long)(v))
+__device__ unsigned long long g_fin_prof[kFMaxCtas][8];
+#define FINPROF_ADD(slot, t0) \
+  if ((threadIdx.x & 31) == 0) atomicAdd(&g_fin_prof[blockIdx.x % kFMaxCtas][slot], (unsigned long long)(clock64() - (t0)))
 #else
+#define FINPROF_ADD(slot, t0)
 #define FPROF_T0(name)
 #define FPROF_ADD(slot, t0)
 #define FPROF_CNT(slot, v)
 #endif
 
-struct FinTile {
-  int64_t bb, tok0, i0;
-  int nvalid;
-};
-
 struct FusedSmem {
   uint8_t a[kAStages][2][kMB * 128];   // kbar chunk, dims 0-63 | 64-127 (SW128)
   uint8_t b[2][kNRows * 128];          // rotated queries of the tile, same split
   uint32_t phist[kTT][kPBins / 2];     // pilot counts, two 16-bit bins per word
-  uint32_t fin_hist[kFinWarps][512];
-  int32_t sortbuf[kFinWarps][kFMaxKb];  // k_B winners before sorting
   uint32_t tau[kTT];
-  int wcnt[2][4][kTT];                 // entries per (slot, lane quarter, token)
-  FinTile fin[2];
-  int fin_stop[2];
   uint64_t a_full[kAStages], a_empty[kAStages];
   uint64_t tfull[2], tempty[2];
   uint64_t b_full, b_empty, pilot_bar, tau_bar, mma_done;
-  uint64_t fin_full[2], fin_empty[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -212,23 +219,33 @@ __device__ __forceinline__ const uint2* entry_ptr(const uint2* seg, int e, int p
   return seg + q * kSeg + off;
 }
 
-// Exact top-k_b of a token's buffer (n entries, k_b <= n <= kFCap, any order):
-// the k_b largest patterns, equal patterns going to the lower block ids; the
-// winners are written to out[] sorted by block id.  One warp.  The patterns
-// stay in registers (entry e = lane + 32 j in slot j); block ids are read back
-// from the buffer only for entries that can win.
+// Exact top-k_b of a token's buffer (n entries, k_b <= n <= kFCap): the k_b
+// largest patterns, equal patterns going to the lower block ids; the winners
+// are written to out[] sorted by block id.  One warp.  The patterns stay in
+// registers (entry e = lane + 32 j in slot j), the block ids in ids[e].  Each
+// segment lists its quarter's blocks in ascending order and the quarters cover
+// consecutive block ranges, so entry order is block order.
 __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int p1, int p2, int p3, int n,
-                                             int k_b, uint32_t* hist, int32_t* sortbuf,
-                                             int32_t* __restrict__ out) {
+                                             int k_b, uint32_t* __restrict__ hist,
+                                             int32_t* __restrict__ ids, int32_t* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   FPROF_T0(f0);
   uint32_t ru[kFinRegs];
 #pragma unroll
-  for (int j = 0; j < kFinRegs; ++j) {
-    const int e = lane + 32 * j;
-    ru[j] = e < n ? __ldcg(&entry_ptr(seg, e, p1, p2, p3)->x) : 0u;
+  for (int j0 = 0; j0 < kFinRegs; j0 += 16) {  // 16 loads in flight per lane
+    uint2 xs[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const int e = lane + 32 * (j0 + jj);
+      xs[jj] = e < n ? __ldcs(entry_ptr(seg, e, p1, p2, p3)) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const int e = lane + 32 * (j0 + jj);
+      ru[j0 + jj] = xs[jj].x;
+      if (e < n) ids[e] = (int32_t)xs[jj].y;
+    }
   }
-  FPROF_T0(f1);
   // Start from the buffer's own pattern range, so the first round's bins are
   // spread over the entries (they all lie within a few octaves of tau).
   uint32_t lo = 0xffffffffu, hi = 0;
@@ -244,24 +261,31 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
     lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
     hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
+  FINPROF_ADD(0, f0);
+  FPROF_T0(f1);
   int need = k_b, mode = (lo == hi) ? 2 : 0;
   for (int guard = 0; mode == 0 && guard < 6; ++guard) {  // the range shrinks 2^9-fold per round
     const int shift = range_shift(lo, hi);
-    for (int j = lane; j < 512; j += 32) hist[j] = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) reinterpret_cast<uint4*>(hist)[lane + 32 * j] = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < kFinRegs; ++j)
       if (lane + 32 * j < n && ru[j] >= lo && ru[j] <= hi) atomicAdd(&hist[(ru[j] - lo) >> shift], 1u);
     refine_round(hist, lo, hi, need, mode, shift);
+#ifdef QSA_FUSED_PROF
+    if (lane == 0) atomicAdd(&g_fin_prof[blockIdx.x % kFMaxCtas][6], 1ull);
+#endif
   }
-  if ((threadIdx.x & 127) == 0) FPROF_ADD(4, f1);
+  __syncwarp();
+  FINPROF_ADD(1, f1);
   FPROF_T0(f2);
   // Ties at a single value: keep the `need` lowest block ids among them.
   uint32_t tie_cut = 0xffffffffu;  // tied entries with block id < tie_cut win
   if (mode == 2) {
-    // Rare path (exact ties at the boundary): re-read the entries from memory.
     int nt = 0;
-    for (int e = lane; e < n; e += 32) nt += (__ldcg(&entry_ptr(seg, e, p1, p2, p3)->x) == lo) ? 1 : 0;
+#pragma unroll
+    for (int j = 0; j < kFinRegs; ++j) nt += (lane + 32 * j < n && ru[j] == lo) ? 1 : 0;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o);
     if (nt > need) {
@@ -273,10 +297,11 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
         const int shift = range_shift(blo, bhi);
         for (int j = lane; j < 512; j += 32) hist[j] = 0;
         __syncwarp();
-        for (int e = lane; e < n; e += 32) {
-          const uint2 x = __ldcg(entry_ptr(seg, e, p1, p2, p3));
-          if (x.x == lo) {
-            const uint32_t key = 0x7fffffffu - x.y;
+#pragma unroll
+        for (int j = 0; j < kFinRegs; ++j) {
+          const int e = lane + 32 * j;
+          if (e < n && ru[j] == lo) {
+            const uint32_t key = 0x7fffffffu - (uint32_t)ids[e];
             if (key >= blo && key <= bhi) atomicAdd(&hist[(key - blo) >> shift], 1u);
           }
         }
@@ -287,98 +312,102 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
       tie_cut = 0x7fffffffu - blo + 1u;
     }
   }
-  // Compact the k_b winners into sortbuf (any order); block ids are read back in
-  // batches of 16 entries per lane so their loads overlap.
+  FINPROF_ADD(2, f2);
+  FPROF_T0(f3);
+  // Entry order is block order, so compacting the k_b winners in entry order
+  // lists them sorted.
   int written = 0;
 #pragma unroll
-  for (int j0 = 0; j0 < kFinRegs; j0 += 16) {
-    if (32 * j0 >= n) break;
-    uint32_t ids[16];
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
-      const int e = lane + 32 * (j0 + jj);
-      ids[jj] = e < n ? __ldcg(&entry_ptr(seg, e, p1, p2, p3)->y) : 0u;
+  for (int j = 0; j < kFinRegs; ++j) {
+    if (32 * j >= n) break;
+    const int e = lane + 32 * j;
+    bool win = false;
+    if (e < n) {
+      win = ru[j] > hi || (mode == 1 && ru[j] >= lo);
+      if (!win && mode == 2 && ru[j] == lo) win = (uint32_t)ids[e] < tie_cut;
     }
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
-      const int j = j0 + jj;
-      const int e = lane + 32 * j;
-      bool win = false;
-      if (e < n) {
-        const bool tied = mode == 2 && ru[j] == lo;
-        win = ru[j] > hi || (mode == 1 && ru[j] >= lo) || (tied && ids[jj] < tie_cut);
-      }
-      const unsigned wm = __ballot_sync(0xffffffffu, win);
-      const int pos = written + __popc(wm & ((1u << lane) - 1u));
-      if (win && pos < k_b) sortbuf[pos] = (int32_t)ids[jj];
-      written += __popc(wm);
-    }
+    const unsigned wm = __ballot_sync(0xffffffffu, win);
+    const int pos = written + __popc(wm & ((1u << lane) - 1u));
+    if (win && pos < k_b) out[pos] = ids[e];
+    written += __popc(wm);
   }
+  for (int i = (written < k_b ? written : k_b) + lane; i < k_b; i += 32) out[i] = -1;
   __syncwarp();
-  if ((threadIdx.x & 127) == 0) FPROF_ADD(7, f2);
-  FPROF_T0(f3);
-  // Sort the k_b ids ascending: a 512-key bitonic network in registers, lane L
-  // holding keys 16 L .. 16 L + 15 (padding keys sort last).
-  int key[16];
-#pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    const int i = 16 * lane + q;
-    key[q] = i < k_b ? sortbuf[i] : 0x7fffffff;
-  }
-#pragma unroll
-  for (int size = 2; size <= kFMaxKb; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride >= 16) {
-        const int lx = stride >> 4;  // partner lane distance
-        const bool upper = (lane & lx) != 0;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int i = 16 * lane + q;
-          const bool asc = (i & size) == 0;
-          const int other = __shfl_xor_sync(0xffffffffu, key[q], lx);
-          // lower element keeps the min when ascending
-          const bool keep_min = (asc != upper);
-          key[q] = keep_min ? min(key[q], other) : max(key[q], other);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          if ((q & stride) == 0) {
-            const int i = 16 * lane + q;
-            const bool asc = (i & size) == 0;
-            const int a = key[q], b = key[q + stride];
-            const bool swap = (a > b) == asc;
-            key[q] = swap ? b : a;
-            key[q + stride] = swap ? a : b;
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    const int i = 16 * lane + q;
-    if (i < k_b) out[i] = key[q];
-  }
-  __syncwarp();
-
+  FINPROF_ADD(3, f3);
+#ifdef QSA_FUSED_PROF
+  if (lane == 0) atomicAdd(&g_fin_prof[blockIdx.x % kFMaxCtas][7], 1ull);
+#endif
 }
 
 // ---------------------------------------------------------------------------------------------
+// Threshold of one token from its pilot histogram (one warp): the lowest bin
+// such that the bins from it upward hold at least ceil(1.5 k_B P / c) of the P
+// samples, as the bit pattern of the bin's lower edge (0 when the bottom bin is
+// reached or the row has no samples, which collects every visible block).  The
+// histogram is cleared for the next tile.  Lane L owns bins 16 (31 - L) .. + 15.
+__device__ __forceinline__ uint32_t pilot_tau(uint32_t* __restrict__ hist, int64_t c, int k_b) {
+  const int lane = threadIdx.x & 31;
+  uint4* const w4 = reinterpret_cast<uint4*>(hist + 8 * (31 - lane));
+  const uint4 lo4 = w4[0], hi4 = w4[1];
+  const uint32_t wd[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+  w4[0] = make_uint4(0, 0, 0, 0);
+  w4[1] = make_uint4(0, 0, 0, 0);
+  int loc[16], sum = 0;  // loc[q]: bin 16 (31 - lane) + 15 - q
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int j = 15 - q;
+    loc[q] = (int)((j & 1) ? (wd[j >> 1] >> 16) : (wd[j >> 1] & 0xffffu));
+    sum += loc[q];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int64_t P = __shfl_sync(0xffffffffu, incl, 31);
+  int64_t want = (3 * (int64_t)k_b * P + 2 * c - 1) / (2 * c);  // ceil(1.5 k_B P / c)
+  if (want < 1) want = 1;
+  const int above0 = incl - sum;
+  const bool cross = above0 < want && incl >= want;
+  uint32_t tau = 0;
+  if (cross) {
+    int above = above0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      above += loc[q];
+      if (above >= want) {
+        const int bin = 16 * (31 - lane) + 15 - q;
+        tau = bin == 0 ? 0u : (uint32_t)(kPBase + bin) << kPShift;
+        break;
+      }
+    }
+  }
+  const unsigned who = __ballot_sync(0xffffffffu, cross);
+  return who ? __shfl_sync(0xffffffffu, tau, __ffs(who) - 1) : 0u;
+}
+
+// Tile order of a CTA: the k-th tile it takes is round k of a snake over the
+// launch's tiles, heaviest (latest positions) first, so that the per-CTA sums
+// of the (position-proportional) tile costs stay level.  -1: no tile.
+__device__ __forceinline__ int64_t tile_order(int64_t k, int64_t t_count) {
+  const int64_t G = gridDim.x, b = blockIdx.x;
+  const int64_t kk = k * G + ((k & 1) ? G - 1 - b : b);
+  return kk < t_count ? t_count - 1 - kk : -1;
+}
+
 __global__ void __launch_bounds__(kFThreads, 1)
 index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_kp, const int64_t* __restrict__ q_pos,
-                        int64_t n_q, int64_t tiles_per_seq, int64_t n_tiles, int rshift, int k_b,
-                        int64_t c_cap, int32_t* __restrict__ idx,
-                        int32_t* __restrict__ count, uint2* __restrict__ buf, int64_t* __restrict__ fb_rows,
-                        int* __restrict__ fb_count) {
+                        int64_t n_q, int64_t tiles_per_seq, int64_t t_begin, int64_t t_count, int rshift,
+                        int k_b, int64_t c_cap, uint2* __restrict__ buf, int* __restrict__ cnt) {
   using namespace sm100;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* const smem_base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   FusedSmem& S = *reinterpret_cast<FusedSmem*>(smem_base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &S.abort_flag;
+  const int64_t rounds = (t_count + gridDim.x - 1) / gridDim.x;
   FPROF_T0(t_kernel);
 
   if (threadIdx.x == 0) {
@@ -389,8 +418,6 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     for (int a = 0; a < 2; ++a) {
       mbar_init(&S.tfull[a], 1);
       mbar_init(&S.tempty[a], kEpiWarps);
-      mbar_init(&S.fin_full[a], kEpiWarps);
-      mbar_init(&S.fin_empty[a], kFinWarps);
     }
     mbar_init(&S.b_full, 1);
     mbar_init(&S.b_empty, 1);
@@ -401,7 +428,6 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     fence_mbar_init();
   }
   for (int j = threadIdx.x; j < kTT * (kPBins / 2); j += kFThreads) (&S.phist[0][0])[j] = 0;
-  for (int j = threadIdx.x; j < 2 * 4 * kTT; j += kFThreads) (&S.wcnt[0][0][0])[j] = 0;
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
@@ -421,8 +447,10 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     if (lane == 0) {
       uint32_t it = 0, b_uses = 0;
       bool ok = true;
-      for (int64_t k = blockIdx.x; ok && k < n_tiles; k += gridDim.x) {
-        const TileMeta m = tile_meta(n_tiles - 1 - k, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
+      for (int64_t k = 0; ok && k < rounds; ++k) {
+        const int64_t lt = tile_order(k, t_count);
+        if (lt < 0) continue;
+        const TileMeta m = tile_meta(t_begin + lt, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
         if (!m.mma) continue;
         if (!mbar_wait(&S.b_empty, (b_uses & 1) ^ 1, abort_flag, kWaitCycles, 128)) { ok = false; break; }
         ++b_uses;
@@ -440,9 +468,13 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             tma_load_4d(S.a[st][0], &tm_kp, &S.a_full[st], 0, ph, kc * kMB, (int)m.bb);
             tma_load_4d(S.a[st][1], &tm_kp, &S.a_full[st], 64, ph, kc * kMB, (int)m.bb);
           } else {
-            const int ch = x - m.npilot;
-            tma_load_3d(S.a[st][0], &tm_k, &S.a_full[st], 0, ch * kMB, (int)m.bb);
-            tma_load_3d(S.a[st][1], &tm_k, &S.a_full[st], 64, ch * kMB, (int)m.bb);
+            // Rows 32 q .. 32 q + 31 of the chunk: blocks q R + 32 ch + j of region q.
+            const int ch = x - m.npilot, R = m.nchunks * 32;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              tma_load_3d(S.a[st][0] + q * 4096, &tm_k, &S.a_full[st], 0, q * R + ch * 32, (int)m.bb);
+              tma_load_3d(S.a[st][1] + q * 4096, &tm_k, &S.a_full[st], 64, q * R + ch * 32, (int)m.bb);
+            }
           }
         }
       }
@@ -460,8 +492,10 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       uint32_t it = 0, ct = 0, b_uses = 0;
       bool ok = true;
       const uint32_t b0 = smem_u32(S.b[0]), b1 = smem_u32(S.b[1]);
-      for (int64_t k = blockIdx.x; ok && k < n_tiles; k += gridDim.x) {
-        const TileMeta m = tile_meta(n_tiles - 1 - k, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
+      for (int64_t k = 0; ok && k < rounds; ++k) {
+        const int64_t lt = tile_order(k, t_count);
+        if (lt < 0) continue;
+        const TileMeta m = tile_meta(t_begin + lt, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
         if (!m.mma) continue;
         if (!mbar_wait(&S.b_full, b_uses & 1, abort_flag, kWaitCycles, 64)) { ok = false; break; }
         ++b_uses;
@@ -492,78 +526,48 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       volatile int never = 0;
       mbar_wait(&S.mma_done, 0, &never, 100000000LL);
     }
-  } else if (warp < 2 + kEpiWarps) {
+  } else {
     // ------------------------------------------------------------ score warps
-    const int ew = warp - 2;            // 0..7
+    const int ew = warp - 2;            // 0..15
     const int q4 = warp & 3;            // TMEM lane quarter: blocks 32 q4 .. 32 q4 + 31 of a chunk
-    const int half = ew >> 2;           // columns (tokens) 32 half .. 32 half + 31
-    uint32_t ct = 0, tile_n = 0, pilot_n = 0;
+    const int h = ew >> 2;              // tokens 16 h .. 16 h + 15 (TMEM columns 64 h .. 64 h + 63)
+    const int cap32 = (int)(c_cap < 0x7fffffff ? c_cap : 0x7fffffff);
+    uint32_t ct = 0, pilot_n = 0;
     bool ok = true;
-    for (int64_t k = blockIdx.x; ok && k < n_tiles; k += gridDim.x) {
-      const TileMeta m = tile_meta(n_tiles - 1 - k, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
-      // Rows that keep every visible block (c <= k_B) are written directly by the
-      // warp owning them (tokens 8 ew .. 8 ew + 7).
-      for (int tt = 0; tt < 8; ++tt) {
-        const int t = 8 * ew + tt;
-        if (t >= m.nvalid) break;
-        const int64_t c = token_c(m, t, rshift, c_cap);
-        if (c > k_b) continue;
-        const int64_t grow = m.bb * n_q + m.tok0 + t;
-        int32_t* out = idx + grow * (int64_t)k_b;
-        for (int j = lane; j < k_b; j += 32) out[j] = j < c ? j : -1;
-        if (lane == 0) count[grow] = (int32_t)c;
-      }
+    for (int64_t k = 0; ok && k < rounds; ++k) {
+      const int64_t lt = tile_order(k, t_count);
+      if (lt < 0) continue;
+      const TileMeta m = tile_meta(t_begin + lt, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
       if (!m.mma) continue;
-      const int slot = tile_n & 1;
-      const uint32_t tcol = (uint32_t)(half * 128);
-      // Token 32 half + j sits at position pos32 + j; tokens j >= tlim are past the end.
-      const int pos32 = (int)(m.i0 + 32 * half);
-      const int cap32 = (int)(c_cap < 0x7fffffff ? c_cap : 0x7fffffff);
-      const int cmin32 = min((pos32 + 1) >> rshift, cap32);  // smallest c of the half
+      // Token 16 h + j sits at position pos16 + j.
+      const int pos16 = (int)(m.i0 + 16 * h);
+      const int cmin16 = min((pos16 + 1) >> rshift, cap32);  // smallest c of the warp's tokens
+      // Segment of (token 16 h + j, this warp's lane quarter): seg0 + j * 4 kSeg.
+      uint2* const seg0 = buf + ((lt * kTT + 16 * h) * 4 + q4) * kSeg;
+      // Entry count of token 16 h + lane, held by lanes 0-15.
+      int my_cnt = 0;
       const int total = m.npilot + m.nchunks;
       for (int x = 0; x < total; ++x, ++ct) {
         const bool pilot = x < m.npilot;
         if (x == m.npilot) {
-          // ---- pilot done: thresholds for the tokens this warp owns
+          // ---- pilot done: thresholds of tokens ew, ew + 16, ew + 32, ew + 48
+          FPROF_T0(tt0);
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.pilot_bar);
           if (!warp_wait(&S.pilot_bar, pilot_n & 1, abort_flag)) { ok = false; break; }
-          if (lane < 8) {
-            const int t = 8 * ew + lane;
-            uint32_t tau = 0xffffffffu;  // rows that do not select collect nothing
-            if (t < m.nvalid) {
-              const int64_t c = token_c(m, t, rshift, c_cap);
-              if (c > k_b) {
-                int64_t P = 0;
-                for (int w = 0; w < kPBins / 2; ++w) {
-                  const uint32_t v = S.phist[t][w];
-                  P += (v & 0xffffu) + (v >> 16);
-                }
-                int64_t want = (3 * (int64_t)k_b * P + 2 * c - 1) / (2 * c);  // ceil(1.5 k_B P / c)
-                if (want < 1) want = 1;
-                tau = 0;
-                int64_t acc = 0;
-                for (int bin = kPBins - 1; bin >= 0; --bin) {
-                  const uint32_t v = S.phist[t][bin >> 1];
-                  acc += (bin & 1) ? (v >> 16) : (v & 0xffffu);
-                  if (acc >= want) {
-                    tau = bin == 0 ? 0u : (uint32_t)(kPBase + bin) << kPShift;
-                    break;
-                  }
-                }
-              }
-            }
-            S.tau[t] = tau;
-            for (int w = 0; w < kPBins / 2; ++w) S.phist[t][w] = 0;  // ready for the next tile
+#pragma unroll 1
+          for (int j = 0; j < kTT / 16; ++j) {
+            const int t = ew + 16 * j;
+            const int64_t c = token_c(m, t, rshift, c_cap);
+            // Rows that do not select (past the end, or c <= k_B) collect nothing.
+            const uint32_t tau = pilot_tau(S.phist[t], c, k_b);
+            if (lane == 0) S.tau[t] = (t < m.nvalid && c > k_b) ? tau : 0xffffffffu;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.tau_bar);
           if (!warp_wait(&S.tau_bar, pilot_n & 1, abort_flag)) { ok = false; break; }
+          if (ew == 0 && lane == 0) FPROF_ADD(8, tt0);
           ++pilot_n;
-          // The finalize warps must be done with this buffer slot.
-          FPROF_T0(tf);
-          if (!warp_wait(&S.fin_empty[slot], ((tile_n >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-          if (ew == 0 && lane == 0) FPROF_ADD(8, tf);
         }
         const int acc = ct & 1;
         FPROF_T0(ts);
@@ -572,155 +576,99 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         FPROF_T0(tp);
         tc_fence_after();
 
-        // This lane's block: pilot chunks hold blocks 16 (kMB kc + row) + ph.
-        const int row = 32 * q4 + lane;
-        int bi;            // block id (< 2^31)
-        bool row_ok = true;
-        if (pilot) {
-          const int ph = x / m.mc, kc = x % m.mc;
-          const int grp = kc * kMB + row;
-          bi = grp * kPilotStride + ph;
-          row_ok = grp < m.ngroups;
-        } else {
-          bi = (x - m.npilot) * kMB + row;
-        }
-        // Segment of (token 32 half + j, this warp's lane quarter) in the slot's buffer.
-        uint2* const seg0 = buf + (((int64_t)(blockIdx.x * 2 + slot) * kTT + 32 * half) * 4 + q4) * kSeg;
-        // Every block of this chunk is visible to every token of this warp's half
-        // when the chunk ends below the first token's visible range.
-        const int chunk_last = pilot ? (m.mc * kMB) * kPilotStride : (x - m.npilot + 1) * kMB;
-        const bool chunk_all_visible = chunk_last <= cmin32;
-#pragma unroll 1
-        for (int g = 0; g < 4; ++g) {
-          uint32_t v[32];
-          FPROF_T0(tl);
-          tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(acc * kNRows) + tcol + (uint32_t)(32 * g), v);
-          tmem_ld_wait();
-          if (ew == 0 && lane == 0) FPROF_ADD(14, tl);
-          FPROF_T0(tb);
-          // Scores of the 8 tokens 32 half + 8 g + kk for this lane's block.
-          uint32_t uu[8];
+        // The 64 accumulator columns of this warp's 16 tokens are reduced to
+        // 16 scores in registers (32 columns at a time), and the accumulator is
+        // handed back to the MMA warp at once.  x + |x| is 2 ReLU(x) exactly and
+        // doubling commutes with the rounding of the sums, so the bit patterns
+        // of 2 x score order exactly as the scores do.
+        uint32_t u16[16];
+        FPROF_T0(tl);
+        {
+          const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(acc * kNRows + 64 * h);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const float sc = (fmaxf(__uint_as_float(v[4 * kk]), 0.f) + fmaxf(__uint_as_float(v[4 * kk + 1]), 0.f)) +
-                             (fmaxf(__uint_as_float(v[4 * kk + 2]), 0.f) + fmaxf(__uint_as_float(v[4 * kk + 3]), 0.f));
-            uu[kk] = __float_as_uint(sc) & 0x7fffffffu;
-          }
-          // Which of the 8 tokens see this block.  Tokens that do not select
-          // (past the end, or c <= k_B) are excluded by their threshold; their
-          // pilot counts are never read.
-          uint32_t vis = row_ok ? 0xffu : 0u;
-          if (!chunk_all_visible) {
+          for (int g = 0; g < 2; ++g) {
+            uint32_t v[32];
+            tmem_ld32(taddr + (uint32_t)(32 * g), v);
+            tmem_ld_wait();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              int c = (pos32 + 8 * g + kk + 1) >> rshift;
-              c = c < cap32 ? c : cap32;
-              if (bi >= c) vis &= ~(1u << kk);
+              const float a0 = __uint_as_float(v[4 * kk]), a1 = __uint_as_float(v[4 * kk + 1]);
+              const float a2 = __uint_as_float(v[4 * kk + 2]), a3 = __uint_as_float(v[4 * kk + 3]);
+              u16[8 * g + kk] =
+                  __float_as_uint(((a0 + fabsf(a0)) + (a1 + fabsf(a1))) + ((a2 + fabsf(a2)) + (a3 + fabsf(a3))));
             }
           }
-          const int tg = 32 * half + 8 * g;  // first token of the group
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.tempty[acc]);
+        }
+        if (ew == 0 && lane == 0) FPROF_ADD(14, tl);
+        FPROF_T0(tc);
+        // Blocks of this warp's lanes: main chunk ch holds blocks gbase + lane,
+        // gbase = q4 R + 32 ch (the quarter's own region of R = 32 nchunks
+        // blocks); pilot chunks hold blocks 16 (gbase + lane) + ph, gbase = kMB kc + 32 q4.
+        const int ph = pilot ? x / m.mc : 0;
+        const int gbase = pilot ? (x % m.mc) * kMB + 32 * q4 : q4 * (m.nchunks * 32) + (x - m.npilot) * 32;
+        const int bi = pilot ? (gbase + lane) * kPilotStride + ph : gbase + lane;
+        // Every block of the warp is visible to all 16 tokens when they end
+        // below the first token's visible range.
+        const int warp_last = pilot ? (m.mc * kMB) * kPilotStride : gbase + 32;
+        const bool chunk_all_visible = warp_last <= cmin16;
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const uint32_t* const uu = &u16[8 * g];
+          const int tg = 16 * h + 8 * g;  // first token of the group
+          // Lanes (blocks) each of the 8 tokens sees: a prefix of the warp, as
+          // block ids grow with the lane.  Tokens that do not select are excluded
+          // by their threshold; their pilot counts are never read.
+          auto vis_mask = [&](int kk) -> unsigned {
+            if (chunk_all_visible) return 0xffffffffu;
+            int c = (pos16 + 8 * g + kk + 1) >> rshift;
+            c = c < cap32 ? c : cap32;
+            int lim;
+            if (pilot) {
+              const int ng = c > ph ? (c - ph + kPilotStride - 1) / kPilotStride : 0;
+              lim = (ng < m.ngroups ? ng : m.ngroups) - gbase;
+            } else {
+              lim = c - gbase;
+            }
+            return lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
+          };
           if (pilot) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               int bin = (int)(uu[kk] >> kPShift) - kPBase;
               bin = bin < 0 ? 0 : (bin > kPBins - 1 ? kPBins - 1 : bin);
-              if (vis & (1u << kk)) atomicAdd(&S.phist[tg + kk][bin >> 1], (bin & 1) ? 65536u : 1u);
+              if ((vis_mask(kk) >> lane) & 1u) atomicAdd(&S.phist[tg + kk][bin >> 1], (bin & 1) ? 65536u : 1u);
             }
           } else {
             const uint4 ta = *reinterpret_cast<const uint4*>(&S.tau[tg]);
-            const uint4 tc4 = *reinterpret_cast<const uint4*>(&S.tau[tg + 4]);
-            const uint32_t tauv[8] = {ta.x, ta.y, ta.z, ta.w, tc4.x, tc4.y, tc4.z, tc4.w};
-            const int4 ca = *reinterpret_cast<const int4*>(&S.wcnt[slot][q4][tg]);
-            const int4 cb = *reinterpret_cast<const int4*>(&S.wcnt[slot][q4][tg + 4]);
-            const int base[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-            unsigned tmk[8];
+            const uint4 tb4 = *reinterpret_cast<const uint4*>(&S.tau[tg + 4]);
+            const uint32_t tauv[8] = {ta.x, ta.y, ta.z, ta.w, tb4.x, tb4.y, tb4.z, tb4.w};
+            bool pass = false;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              tmk[kk] = __ballot_sync(0xffffffffu, ((vis >> kk) & 1u) && uu[kk] >= tauv[kk]);
-            const unsigned lt = (1u << lane) - 1u;
+            for (int kk = 0; kk < 8; ++kk) pass |= uu[kk] >= tauv[kk];
+            if (__any_sync(0xffffffffu, pass)) {  // a chunk whose 256 pairs all fall below tau is skipped
+              if (ew == 0 && lane == 0) FPROF_CNT(2, 1);
+              const unsigned lt_mask = (1u << lane) - 1u;
+              int add = 0;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const int pos = base[kk] + __popc(tmk[kk] & lt);
-              if ((tmk[kk] >> lane) & 1u) {
-                if (pos < kSeg) seg0[(int64_t)(8 * g + kk) * 4 * kSeg + pos] = make_uint2(uu[kk], (uint32_t)bi);
+              for (int kk = 0; kk < 8; ++kk) {
+                const unsigned tmk = __ballot_sync(0xffffffffu, uu[kk] >= tauv[kk]) & vis_mask(kk);
+                const int pos = __shfl_sync(0xffffffffu, my_cnt, 8 * g + kk) + __popc(tmk & lt_mask);
+                if (((tmk >> lane) & 1u) && pos < kSeg)
+                  seg0[(8 * g + kk) * 4 * kSeg + pos] = make_uint2(uu[kk], (uint32_t)bi);
+                add = lane == 8 * g + kk ? __popc(tmk) : add;
               }
-            }
-            __syncwarp();
-            if (lane == 0) {
-              *reinterpret_cast<int4*>(&S.wcnt[slot][q4][tg]) =
-                  make_int4(ca.x + __popc(tmk[0]), ca.y + __popc(tmk[1]), ca.z + __popc(tmk[2]), ca.w + __popc(tmk[3]));
-              *reinterpret_cast<int4*>(&S.wcnt[slot][q4][tg + 4]) =
-                  make_int4(cb.x + __popc(tmk[4]), cb.y + __popc(tmk[5]), cb.z + __popc(tmk[6]), cb.w + __popc(tmk[7]));
+              my_cnt += add;
             }
           }
-          if (ew == 0 && lane == 0) { FPROF_ADD(pilot ? 1 : 15, tb); FPROF_CNT(pilot ? 0 : 2, 1); }
         }
-        FPROF_T0(tz);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.tempty[acc]);
-        if (ew == 0 && lane == 0) { FPROF_ADD(6, tp); FPROF_ADD(13, tz); }
+        if (ew == 0 && lane == 0) { FPROF_ADD(6, tp); FPROF_ADD(pilot ? 1 : 15, tc); FPROF_CNT(pilot ? 0 : 13, 1); }
       }
       if (!ok) break;
-      // ---- hand the tile's buffers to the finalize warps
-      if (ew == 0 && lane == 0) {
-        FinTile ft;
-        ft.bb = m.bb; ft.tok0 = m.tok0; ft.i0 = m.i0; ft.nvalid = m.nvalid;
-        S.fin[slot] = ft;
-        S.fin_stop[slot] = 0;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.fin_full[slot]);
-      ++tile_n;
-    }
-    // Stop the finalize warps.
-    if (ok) {
-      const int slot = tile_n & 1;
-      if (warp_wait(&S.fin_empty[slot], ((tile_n >> 1) & 1) ^ 1, abort_flag)) {
-        if (ew == 0 && lane == 0) S.fin_stop[slot] = 1;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.fin_full[slot]);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ finalize warps
-    const int fw = warp - 2 - kEpiWarps;
-    uint32_t fc = 0;
-    while (true) {
-      const int slot = fc & 1;
-      FPROF_T0(tq);
-      if (!warp_wait(&S.fin_full[slot], (fc >> 1) & 1, abort_flag, 256)) break;
-      if (fw == 0 && lane == 0) FPROF_ADD(9, tq);
-      if (*(volatile int*)&S.fin_stop[slot]) break;
-      FPROF_T0(tr);
-      const FinTile ft = S.fin[slot];
-      for (int t = fw; t < kTT; t += kFinWarps) {
-        const int n0 = S.wcnt[slot][0][t], n1 = S.wcnt[slot][1][t];
-        const int n2 = S.wcnt[slot][2][t], n3 = S.wcnt[slot][3][t];
-        const int n = n0 + n1 + n2 + n3;
-        const bool seg_ok = n0 <= kSeg && n1 <= kSeg && n2 <= kSeg && n3 <= kSeg;
-        if (t < ft.nvalid) {
-          int64_t c = (ft.i0 + t + 1) >> rshift;
-          if (c > c_cap) c = c_cap;
-          if (c > k_b) {
-            const int64_t grow = ft.bb * n_q + ft.tok0 + t;
-            if (seg_ok && n >= k_b && n <= kFCap) {
-              const uint2* seg = buf + ((int64_t)(blockIdx.x * 2 + slot) * kTT + t) * 4 * kSeg;
-              finalize_row(seg, n0, n0 + n1, n0 + n1 + n2, n, k_b, S.fin_hist[fw], S.sortbuf[fw],
-                           idx + grow * (int64_t)k_b);
-              if (lane == 0) count[grow] = k_b;
-            } else if (lane == 0) {
-              fb_rows[atomicAdd(fb_count, 1)] = grow;  // the exact fallback kernel takes it
-            }
-          }
-        }
-        __syncwarp();
-        if (lane < 4) S.wcnt[slot][lane][t] = 0;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.fin_empty[slot]);
-      if (fw == 0 && lane == 0) FPROF_ADD(10, tr);
-      ++fc;
+      // ---- tile done: this warp's entry counts go to the finalize kernel
+      if (lane < 16) cnt[(lt * 4 + q4) * kTT + 16 * h + lane] = my_cnt;
     }
   }
 
@@ -730,6 +678,50 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Selection of every query row of a launch's tiles, one warp per row: rows that
+// see at most k_B blocks keep all of them (-1 padding); the others take the
+// exact top-k_B of the entries their tile collected (finalize_row), or are
+// queued for the exact fallback kernel when their buffer fell outside
+// [k_B, kFCap] entries or a segment overflowed.
+__global__ void __launch_bounds__(32 * kFinKWarps, 3)
+index_finalize_kernel(const uint2* __restrict__ buf, const int* __restrict__ cnt, const int64_t* __restrict__ q_pos,
+                      int64_t n_q, int64_t tiles_per_seq, int64_t t_begin, int64_t t_count, int rshift, int k_b,
+                      int64_t c_cap, int32_t* __restrict__ idx, int32_t* __restrict__ count,
+                      int64_t* __restrict__ fb_rows, int* __restrict__ fb_count) {
+  __shared__ __align__(16) uint32_t hist[kFinKWarps][512];
+  __shared__ int32_t ids[kFinKWarps][kFCap];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t rows = t_count * kTT;
+  for (int64_t rr = (int64_t)blockIdx.x * kFinKWarps + w; rr < rows; rr += (int64_t)gridDim.x * kFinKWarps) {
+    const int64_t lt = rr / kTT;
+    const int t = (int)(rr % kTT);
+    const int64_t tile = t_begin + lt;
+    const int64_t bb = tile / tiles_per_seq;
+    const int64_t tok = (tile % tiles_per_seq) * kTT + t;
+    if (tok >= n_q) continue;
+    int64_t c = (q_pos[bb] + tok + 1) >> rshift;
+    if (c > c_cap) c = c_cap;
+    const int64_t grow = bb * n_q + tok;
+    int32_t* const out = idx + grow * (int64_t)k_b;
+    if (c <= k_b) {
+      for (int j = lane; j < k_b; j += 32) out[j] = j < c ? j : -1;
+      if (lane == 0) count[grow] = (int32_t)c;
+      continue;
+    }
+    const int* const cr = cnt + lt * 4 * kTT + t;
+    const int n0 = cr[0], n1 = cr[kTT], n2 = cr[2 * kTT], n3 = cr[3 * kTT];
+    const int n = n0 + n1 + n2 + n3;
+    const bool seg_ok = n0 <= kSeg && n1 <= kSeg && n2 <= kSeg && n3 <= kSeg;
+    if (seg_ok && n >= k_b && n <= kFCap) {
+      finalize_row(buf + (lt * kTT + t) * 4 * kSeg, n0, n0 + n1, n0 + n1 + n2, n, k_b, hist[w], ids[w], out);
+      if (lane == 0) count[grow] = k_b;
+    } else if (lane == 0) {
+      fb_rows[atomicAdd(fb_count, 1)] = grow;  // the exact fallback kernel takes it
+    }
   }
 }
 
@@ -802,21 +794,23 @@ index_fallback_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16*
 // Host side
 
 struct FusedLayout {
-  int64_t tiles_per_seq, n_tiles;
-  size_t buf_off, fb_rows_off, fb_count_off, scratch_off, total;
+  int64_t tiles_per_seq, n_tiles, tiles_per_launch;
+  size_t buf_off, cnt_off, fb_rows_off, fb_count_off, scratch_off, total;
   int64_t scratch_stride;
 };
 
-// Workspace of the fused path (after the rotated queries): per-CTA token
-// buffers (2 slots x 64 tokens x 4 segments x kSeg entries), the fallback row list and
-// counter, and the fallback kernel's score rows.
+// Workspace of the fused path (after the rotated queries): the entry buffers of
+// one launch's tiles (64 tokens x 4 segments x kSeg entries per tile) and their
+// counts, the fallback row list and counter, and the fallback kernel's score rows.
 inline FusedLayout fused_layout(int64_t B, int64_t n_q, int64_t n_blocks_max) {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
   FusedLayout L;
   L.tiles_per_seq = (n_q + kTT - 1) / kTT;
   L.n_tiles = B * L.tiles_per_seq;
+  L.tiles_per_launch = L.n_tiles < kTilesPerLaunch ? L.n_tiles : kTilesPerLaunch;
   L.buf_off = 0;
-  L.fb_rows_off = al(L.buf_off + (size_t)kFMaxCtas * 2 * kTT * 4 * kSeg * sizeof(uint2));
+  L.cnt_off = al(L.buf_off + (size_t)L.tiles_per_launch * kTT * 4 * kSeg * sizeof(uint2));
+  L.fb_rows_off = al(L.cnt_off + (size_t)L.tiles_per_launch * 4 * kTT * sizeof(int));
   L.fb_count_off = al(L.fb_rows_off + (size_t)B * n_q * sizeof(int64_t));
   L.scratch_off = al(L.fb_count_off + sizeof(int));
   L.scratch_stride = (n_blocks_max + 63) / 64 * 64;
@@ -866,7 +860,7 @@ cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kba
     if (B == 1 || sb < nb * kHeadDim) sb = nb * kHeadDim;
     const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)nb, (cuuint64_t)B};
     const cuuint64_t strides[2] = {kHeadDim * 2, (cuuint64_t)sb * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kMB, 1};
+    const cuuint32_t box[3] = {64, 32, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(kbar), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -898,6 +892,9 @@ cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kba
     attr_set = true;
   }
   int* fb_count = reinterpret_cast<int*>(w + L.fb_count_off);
+  int64_t* fb_rows = reinterpret_cast<int64_t*>(w + L.fb_rows_off);
+  uint2* buf = reinterpret_cast<uint2*>(w + L.buf_off);
+  int* cnt = reinterpret_cast<int*>(w + L.cnt_off);
   cudaError_t e = cudaMemsetAsync(fb_count, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -905,18 +902,28 @@ cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kba
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  int64_t grid = sms < kFMaxCtas ? sms : kFMaxCtas;
-  if (grid > L.n_tiles) grid = L.n_tiles;
   int rshift = 0;  // r is a power of two
   while ((1 << rshift) < r) ++rshift;
-  index_topk_fused_kernel<<<(unsigned)grid, kFThreads, kFusedSmemBytes, st>>>(
-      tm_q, tm_k, tm_kp, q_pos, n_q, L.tiles_per_seq, L.n_tiles, rshift, k_b, n_blocks_max, idx, count,
-      reinterpret_cast<uint2*>(w + L.buf_off), reinterpret_cast<int64_t*>(w + L.fb_rows_off), fb_count);
-  e = count_launch(cudaGetLastError());
-  if (e != cudaSuccess) return e;
+  // Launches over ranges of tiles, the last (heaviest) range first.
+  for (int64_t t_end = L.n_tiles; t_end > 0; t_end -= L.tiles_per_launch) {
+    const int64_t t_begin = t_end > L.tiles_per_launch ? t_end - L.tiles_per_launch : 0;
+    const int64_t t_count = t_end - t_begin;
+    int64_t grid = sms < kFMaxCtas ? sms : kFMaxCtas;
+    if (grid > t_count) grid = t_count;
+    index_topk_fused_kernel<<<(unsigned)grid, kFThreads, kFusedSmemBytes, st>>>(
+        tm_q, tm_k, tm_kp, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, n_blocks_max, buf, cnt);
+    e = count_launch(cudaGetLastError());
+    if (e != cudaSuccess) return e;
+    const int64_t fin_blocks = (t_count * kTT + kFinKWarps - 1) / kFinKWarps;
+    index_finalize_kernel<<<(unsigned)fin_blocks, 32 * kFinKWarps, 0, st>>>(
+        buf, cnt, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, n_blocks_max, idx, count, fb_rows,
+        fb_count);
+    e = count_launch(cudaGetLastError());
+    if (e != cudaSuccess) return e;
+  }
   index_fallback_kernel<<<kFbCtas, kSelThreads, 0, st>>>(
-      qt, kbar, kbar_stride_b, q_pos, n_q, r, k_b, n_blocks_max, reinterpret_cast<int64_t*>(w + L.fb_rows_off),
-      fb_count, reinterpret_cast<float*>(w + L.scratch_off), L.scratch_stride, idx, count);
+      qt, kbar, kbar_stride_b, q_pos, n_q, r, k_b, n_blocks_max, fb_rows, fb_count,
+      reinterpret_cast<float*>(w + L.scratch_off), L.scratch_stride, idx, count);
   return count_launch(cudaGetLastError());
 }
 
@@ -926,6 +933,14 @@ extern "C" int qsa_debug_fused_prof(unsigned long long* host, int reset) {
   if (reset) {
     static unsigned long long zeros[kFMaxCtas][16] = {};
     if (cudaMemcpyToSymbol(g_fused_prof, zeros, sizeof(zeros)) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+extern "C" int qsa_debug_fin_prof(unsigned long long* host, int reset) {
+  if (cudaMemcpyFromSymbol(host, g_fin_prof, sizeof(g_fin_prof)) != cudaSuccess) return 1;
+  if (reset) {
+    static unsigned long long zeros[kFMaxCtas][8] = {};
+    if (cudaMemcpyToSymbol(g_fin_prof, zeros, sizeof(zeros)) != cudaSuccess) return 1;
   }
   return 0;
 }

@@ -288,6 +288,69 @@ def test_decode_full_size_sampled_sequences():
         check_decode_seq(cfg, wl, bb, idx, cnt, out, lse)
 
 
+@pytest.mark.slow
+def test_long_context_chunk_rows_past_bitmap_range():
+    """A 128-row chunk at positions 135000.. of a drift workload: every row sees
+    more than 32768 blocks, so its winners are ordered by merging the sorted
+    segments rather than through the block bitmap."""
+    spec = PrefillSpec("long_chunk", n=135128, k_tokens=2048, seed=21, drift=True)
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    lo, hi = 135000, 135128
+    assert (lo + 1) // cfg.r > 32768
+    gpu = run_prefill(cfg, wl, q_pos0=lo, rows=slice(lo, hi))
+    rows = [0, 1, 2, 31, 63, 64, 100, 126, 127]
+    res = QC.oracle_rows({**wl, "q_idx": wl["q_idx"][:, lo:hi], "q": wl["q"][:, lo:hi]}, rows, cfg=cfg, q_pos0=lo)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, cfg.r)
+    assert st["exact"] >= len(rows) - 1, st
+
+
+@pytest.mark.slow
+def test_million_token_prefill_sampled_rows():
+    """The 2^20-token needle workload end to end (index + attention on the GPU),
+    checked on sampled rows; results stay on the device and only the sampled
+    rows are copied back."""
+    spec = WORKLOADS["needle_prefill_1m"]
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    n, nb = spec.n, spec.n // spec.r
+    kbar = torch.empty((1, nb, 128), dtype=torch.bfloat16, device=DEV)
+    qsa.qsa_compress_keys(cfg, wl["k_idx"], 0, nb, kbar)
+    q_pos = torch.zeros((1,), dtype=torch.int64, device=DEV)
+    idx = torch.empty((1, n, cfg.k_b), dtype=torch.int32, device=DEV)
+    cnt = torch.empty((1, n), dtype=torch.int32, device=DEV)
+    ws = torch.empty((qsa.qsa_index_topk_workspace(cfg, 1, n, nb),), dtype=torch.uint8, device=DEV)
+    qsa.qsa_index_topk(cfg, wl["q_idx"], kbar, q_pos, nb, idx, cnt, ws)
+    del ws
+    out = torch.empty_like(wl["q"])
+    lse = torch.empty(wl["q"].shape[:3], dtype=torch.float32, device=DEV)
+    qsa.qsa_sparse_attn_prefill(cfg, wl["q"], wl["k"], wl["v"], q_pos, idx, cnt, out, lse)
+    torch.cuda.synchronize()
+    assert qsa.qsa_read_device_error() == 0
+    k_idx = QC.bf16_to_np(wl["k_idx"][0])
+    kb_o = O.compress_keys(k_idx, cfg.r, rope_dims=cfg.rope_dims, rope_base=cfg.rope_base)
+    # Within one bf16 ulp, except where the rotation cancels to far below the
+    # row's scale: there the fp32 rounding of the products (~2^-24 of the
+    # operands) decides, a few 2^-20 of the row's largest entry at most.
+    g = kbar[0].float().cpu().numpy().astype(np.float64)
+    err = np.abs(g - kb_o)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(kb_o), 1e-30))) - 7)
+    row_scale = np.abs(kb_o).max(axis=1, keepdims=True)
+    assert np.all(err <= ulp + 2.0 ** -20 * row_scale), float((err / (ulp + 2.0 ** -20 * row_scale)).max())
+    k, v = QC.bf16_to_np32(wl["k"][0]), QC.bf16_to_np32(wl["v"][0])
+    needle_rows = [i for (_, i, _) in wl["needles"]][:16]
+    rows = QC.sample_rows(n, cfg.k_b, cfg.r, needle_rows, 16, seed=spec.seed)
+    exact = 0
+    for i in rows:
+        res = O.prefill_rows(QC.bf16_to_np32(wl["q_idx"][0, i:i + 1]), None, QC.bf16_to_np32(wl["q"][0, i:i + 1]),
+                             k, v, [0], r=cfg.r, k_tokens=cfg.k_tokens, q_pos0=i, rope_dims=cfg.rope_dims,
+                             rope_base=cfg.rope_base, kbar=kb_o)
+        st = QC.compare_prefill(res, idx[0, i:i + 1].cpu().numpy(), cnt[0, i:i + 1].cpu().numpy(),
+                                out[0, i:i + 1].float().cpu().numpy(), lse[0, i:i + 1].cpu().numpy(), cfg.k_b, cfg.r)
+        exact += st["exact"]
+    assert exact >= 0.9 * len(rows), (exact, len(rows))
+
+
 # ----------------------------------------------------------------------------- full-size prefill, sampled rows
 
 @pytest.mark.slow
