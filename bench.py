@@ -33,6 +33,22 @@ DECODE = "decode_256k_x64"
 L2_FLUSH_BYTES = 256 << 20
 
 
+def reduce_max_over_ranks(vals, world: int, device):
+    """Element-wise max of per-rank timings over all ranks: the slowest rank sets
+    the job's time.  With one rank the values come back unchanged."""
+    import torch
+    t = torch.tensor(list(vals), dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, prefill_ms: float) -> float:
+    """Whole-job prefill throughput: every rank runs its own replica of the
+    workload (weak scaling), timed by the slowest rank."""
+    return world * tokens_per_rank / (prefill_ms * 1e-3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -308,11 +324,8 @@ def main():
     prefill_ms = mean["compress"] + mean["index_prefill"] + mean["attn_prefill"]
     decode_ms = mean["index_decode"] + mean["attn_decode"]
     step_ms = prefill_ms + decode_ms
-    t = torch.tensor([prefill_ms, decode_ms, step_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    prefill_ms, decode_ms, step_ms = t.tolist()
-    value = world * pspec.n / (prefill_ms * 1e-3)
+    prefill_ms, decode_ms, step_ms = reduce_max_over_ranks([prefill_ms, decode_ms, step_ms], world, dev)
+    value = job_tokens_per_s(world, pspec.n, prefill_ms)
 
     # Roofline of each part (algorithmic work / measured mean duration).
     pw = prefill_work(pspec.n, pspec.r, pspec.k_b, pspec.hq, pspec.hkv)
