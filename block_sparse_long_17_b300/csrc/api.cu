@@ -166,7 +166,7 @@ qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* 
     e = launch_decode_scan(qt, static_cast<const __nv_bfloat16*>(kbar), kbar_stride_b, q_pos, B, r, n_blocks_max,
                            S, L.s_stride, st);
     if (e != cudaSuccess) return from_cuda(e);
-    return from_cuda(launch_topk_select_fast(S, L.s_stride, q_pos, n_q, 0, rows, r, k_b, n_blocks_max, idx, count, st));
+    return from_cuda(launch_topk_select_cluster(S, L.s_stride, q_pos, n_q, 0, rows, r, k_b, n_blocks_max, idx, count, st));
   }
   for (int64_t lo = 0; lo < rows; lo += L.rows_per_launch) {
     const int64_t nr = rows - lo < L.rows_per_launch ? rows - lo : L.rows_per_launch;

@@ -133,73 +133,82 @@ cudaError_t launch_index_scan(const __nv_bfloat16* qt, const __nv_bfloat16* kbar
 }
 
 
-// Decode scan: one query row per sequence.  One warp covers kScanChunk blocks
-// of one sequence; the 16-block tiles are double-buffered in registers (the
-// next tile's 8 loads per lane are in flight while the current tile's MMAs
-// run).  MMA columns 0-3 are the 4 indexer heads, 4-7 are zero.
+// Decode scan: one query row per sequence.  A persistent grid of warps splits
+// the (sequence, 16-block tile) space into equal contiguous ranges, so every
+// warp streams the same number of k-bar rows and none is left for a tail wave.
+// Within a range the 16-block tiles are double-buffered in registers (the next
+// tile's 8 loads per lane are in flight while the current tile's MMAs run).
+// MMA columns 0-3 are the 4 indexer heads, 4-7 are zero.
 __global__ void __launch_bounds__(kScanWarps * 32)
 decode_scan_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16* __restrict__ kbar,
                    int64_t kbar_stride_b, const int64_t* __restrict__ q_pos, int64_t B, int r,
-                   int64_t c_cap, int64_t n_chunks, float* __restrict__ S, int64_t s_stride) {
+                   int64_t c_cap, int64_t tiles_per_seq, int64_t tiles_per_warp, float* __restrict__ S,
+                   int64_t s_stride) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, t = lane & 3;
-  const int64_t item = (int64_t)blockIdx.x * kScanWarps + warp;
-  if (item >= B * n_chunks) return;
-  const int64_t bb = item / n_chunks;
-  const int64_t chunk = item % n_chunks;
-  int64_t c = (q_pos[bb] + 1) / r;
-  if (c > c_cap) {
-    if (chunk == 0 && lane == 0) flag_device_error(kDevErrPosition);
-    c = c_cap;
-  }
-  const int64_t b_begin = chunk * kScanChunk;
-  if (b_begin >= c) return;
-  const int64_t b_end = (b_begin + kScanChunk < c) ? b_begin + kScanChunk : c;
-  uint32_t qf[16];
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(qt + (bb * kIdxHeads + (gid & 3)) * kHeadDim + 32 * t);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint4 v = gid < 4 ? src[u] : make_uint4(0, 0, 0, 0);
-      qf[4 * u + 0] = v.x; qf[4 * u + 1] = v.y; qf[4 * u + 2] = v.z; qf[4 * u + 3] = v.w;
+  const int64_t wid = (int64_t)blockIdx.x * kScanWarps + warp;
+  const int64_t total = B * tiles_per_seq;
+  int64_t t0 = wid * tiles_per_warp;
+  const int64_t t1 = t0 + tiles_per_warp < total ? t0 + tiles_per_warp : total;
+  while (t0 < t1) {
+    const int64_t bb = t0 / tiles_per_seq;
+    const int64_t seg_end = (bb + 1) * tiles_per_seq < t1 ? (bb + 1) * tiles_per_seq : t1;
+    int64_t c = (q_pos[bb] + 1) / r;
+    if (c > c_cap) {
+      if (lane == 0 && t0 == bb * tiles_per_seq) flag_device_error(kDevErrPosition);
+      c = c_cap;
     }
-  }
-  const __nv_bfloat16* kb = kbar + bb * kbar_stride_b;
-  float* srow = S + bb * s_stride;
-  auto load_tile = [&](int64_t b0, uint32_t (&ka)[16], uint32_t (&kx)[16]) {
-    const int64_t ra = b0 + gid < b_end ? b0 + gid : b_end - 1;
-    const int64_t rb = b0 + gid + 8 < b_end ? b0 + gid + 8 : b_end - 1;
-    const uint4* pa = reinterpret_cast<const uint4*>(kb + ra * kHeadDim + 32 * t);
-    const uint4* pb = reinterpret_cast<const uint4*>(kb + rb * kHeadDim + 32 * t);
+    const int64_t b_begin = (t0 - bb * tiles_per_seq) * 16;
+    const int64_t b_lim = (seg_end - bb * tiles_per_seq) * 16;
+    const int64_t b_end = b_lim < c ? b_lim : c;
+    t0 = seg_end;
+    if (b_begin >= b_end) continue;
+    uint32_t qf[16];
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(qt + (bb * kIdxHeads + (gid & 3)) * kHeadDim + 32 * t);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint4 x = ldg_stream(pa + u), y = ldg_stream(pb + u);
-      ka[4 * u] = x.x; ka[4 * u + 1] = x.y; ka[4 * u + 2] = x.z; ka[4 * u + 3] = x.w;
-      kx[4 * u] = y.x; kx[4 * u + 1] = y.y; kx[4 * u + 2] = y.z; kx[4 * u + 3] = y.w;
+      for (int u = 0; u < 4; ++u) {
+        const uint4 v = gid < 4 ? src[u] : make_uint4(0, 0, 0, 0);
+        qf[4 * u + 0] = v.x; qf[4 * u + 1] = v.y; qf[4 * u + 2] = v.z; qf[4 * u + 3] = v.w;
+      }
     }
-  };
-  uint32_t ka[16], kx[16], na[16], nx[16];
-  load_tile(b_begin, ka, kx);
-  for (int64_t b0 = b_begin; b0 < b_end; b0 += 16) {
-    const bool more = b0 + 16 < b_end;
-    if (more) load_tile(b0 + 16, na, nx);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const __nv_bfloat16* kb = kbar + bb * kbar_stride_b;
+    float* srow = S + bb * s_stride;
+    auto load_tile = [&](int64_t b0, uint32_t (&ka)[16], uint32_t (&kx)[16]) {
+      const int64_t ra = b0 + gid < b_end ? b0 + gid : b_end - 1;
+      const int64_t rb = b0 + gid + 8 < b_end ? b0 + gid + 8 : b_end - 1;
+      const uint4* pa = reinterpret_cast<const uint4*>(kb + ra * kHeadDim + 32 * t);
+      const uint4* pb = reinterpret_cast<const uint4*>(kb + rb * kHeadDim + 32 * t);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t a[4] = {ka[2 * ks], kx[2 * ks], ka[2 * ks + 1], kx[2 * ks + 1]};
-      const uint32_t b[2] = {qf[2 * ks], qf[2 * ks + 1]};
-      mma_bf16_16816(acc, a, b);
-    }
-    // acc: (block b0+gid, heads 2t, 2t+1), (b0+gid+8, heads 2t, 2t+1); heads >= 4 are zero.
-    float sa = fmaxf(acc[0], 0.f) + fmaxf(acc[1], 0.f);
-    float sb = fmaxf(acc[2], 0.f) + fmaxf(acc[3], 0.f);
-    sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-    sb += __shfl_xor_sync(0xffffffffu, sb, 1);
-    if (t == 0 && b0 + gid < b_end) srow[b0 + gid] = sa;
-    if (t == 0 && b0 + gid + 8 < b_end) srow[b0 + gid + 8] = sb;
-    if (more) {
+      for (int u = 0; u < 4; ++u) {
+        const uint4 x = ldg_stream(pa + u), y = ldg_stream(pb + u);
+        ka[4 * u] = x.x; ka[4 * u + 1] = x.y; ka[4 * u + 2] = x.z; ka[4 * u + 3] = x.w;
+        kx[4 * u] = y.x; kx[4 * u + 1] = y.y; kx[4 * u + 2] = y.z; kx[4 * u + 3] = y.w;
+      }
+    };
+    uint32_t ka[16], kx[16], na[16], nx[16];
+    load_tile(b_begin, ka, kx);
+    for (int64_t b0 = b_begin; b0 < b_end; b0 += 16) {
+      const bool more = b0 + 16 < b_end;
+      if (more) load_tile(b0 + 16, na, nx);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int u = 0; u < 16; ++u) { ka[u] = na[u]; kx[u] = nx[u]; }
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t a[4] = {ka[2 * ks], kx[2 * ks], ka[2 * ks + 1], kx[2 * ks + 1]};
+        const uint32_t b[2] = {qf[2 * ks], qf[2 * ks + 1]};
+        mma_bf16_16816(acc, a, b);
+      }
+      // acc: (block b0+gid, heads 2t, 2t+1), (b0+gid+8, heads 2t, 2t+1); heads >= 4 are zero.
+      float sa = fmaxf(acc[0], 0.f) + fmaxf(acc[1], 0.f);
+      float sb = fmaxf(acc[2], 0.f) + fmaxf(acc[3], 0.f);
+      sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+      sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+      if (t == 0 && b0 + gid < b_end) srow[b0 + gid] = sa;
+      if (t == 0 && b0 + gid + 8 < b_end) srow[b0 + gid + 8] = sb;
+      if (more) {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) { ka[u] = na[u]; kx[u] = nx[u]; }
+      }
     }
   }
 }
@@ -208,11 +217,26 @@ cudaError_t launch_decode_scan(const __nv_bfloat16* qt, const __nv_bfloat16* kba
                                const int64_t* q_pos, int64_t B, int r, int64_t c_max, float* S,
                                int64_t s_stride, cudaStream_t st) {
   if (B <= 0 || c_max <= 0) return cudaSuccess;
-  const int64_t n_chunks = (c_max + kScanChunk - 1) / kScanChunk;
-  const int64_t items = B * n_chunks;
-  const int64_t grid = (items + kScanWarps - 1) / kScanWarps;
+  static int blocks_per_sm = 0;
+  if (blocks_per_sm == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, decode_scan_kernel,
+                                                                  kScanWarps * 32, 0);
+    if (e != cudaSuccess) return e;
+    if (blocks_per_sm < 1) blocks_per_sm = 1;
+  }
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles_per_seq = (c_max + 15) / 16;
+  const int64_t total = B * tiles_per_seq;
+  int64_t warps = (int64_t)sms * blocks_per_sm * kScanWarps;
+  const int64_t tiles_per_warp = (total + warps - 1) / warps;
+  warps = (total + tiles_per_warp - 1) / tiles_per_warp;
+  const int64_t grid = (warps + kScanWarps - 1) / kScanWarps;
   decode_scan_kernel<<<(unsigned)grid, kScanWarps * 32, 0, st>>>(qt, kbar, kbar_stride_b, q_pos, B, r, c_max,
-                                                                 n_chunks, S, s_stride);
+                                                                 tiles_per_seq, tiles_per_warp, S, s_stride);
   return count_launch(cudaGetLastError());
 }
 

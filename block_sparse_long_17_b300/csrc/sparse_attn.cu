@@ -283,19 +283,72 @@ sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
   }
 }
 
-// Decode partials: persistent warps over (sequence, kv head, 8-head chunk,
-// split of kDecodeSplit slots) items.  Writes unnormalised O (fp32) with its
-// running max and sum per head.
-constexpr int kDecodeSplit = 128;
+// Decode: persistent warps over (sequence, kv head, 8-head chunk, split)
+// items; a split is `split_len` consecutive slots.  A warp writes unnormalised O
+// (fp32) with its running max and sum per head, then counts itself in the
+// unit's counter; the warp that completes the count combines the unit's
+// splits (log-sum-exp weights) into the bf16 output and resets the counter.
+constexpr int kDecodeMinSplit = 128;  // fewest slots per split
+
+// Combine of one (sequence, kv head, head chunk) by one warp.  Lane L owns
+// dims 4L .. 4L + 3 of all 8 heads; every lane reads the splits' maxima and
+// sums (the same 64-byte rows, broadcast) and its 8 float4 of each split, all
+// loads independent, so the combine costs about one round trip to L2.
+__device__ void combine_unit(const float* __restrict__ po_unit, const float* __restrict__ pml_unit, int n_split,
+                             int n_heads, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  float mmax[8], L[8];
+  float4 acc[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    mmax[h] = -INFINITY;
+    L[h] = 0.f;
+    acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll 4
+  for (int sp = 0; sp < n_split; ++sp) {
+    const float4* ml4 = reinterpret_cast<const float4*>(pml_unit + sp * 16);
+    const float4 m0 = __ldcg(ml4), m1 = __ldcg(ml4 + 1);
+    const float ms[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+    for (int h = 0; h < 8; ++h) mmax[h] = fmaxf(mmax[h], ms[h]);
+  }
+#pragma unroll 2
+  for (int sp = 0; sp < n_split; ++sp) {
+    const float4* ml4 = reinterpret_cast<const float4*>(pml_unit + sp * 16);
+    const float4 m0 = __ldcg(ml4), m1 = __ldcg(ml4 + 1), l0 = __ldcg(ml4 + 2), l1 = __ldcg(ml4 + 3);
+    const float ms[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    const float ls[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+    float4 x[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+      x[h] = __ldcg(reinterpret_cast<const float4*>(po_unit + (sp * 8 + h) * kHeadDim) + lane);
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const float w = ms[h] > -INFINITY ? exp2f(ms[h] - mmax[h]) : 0.f;
+      L[h] += w * ls[h];
+      acc[h].x += w * x[h].x; acc[h].y += w * x[h].y; acc[h].z += w * x[h].z; acc[h].w += w * x[h].w;
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    if (h < n_heads) {
+      const float inv = L[h] > 0.f ? 1.f / L[h] : 0.f;  // L = 0 only for a rejected cache length
+      const uint2 pk = make_uint2(pack_bf16x2(acc[h].x * inv, acc[h].y * inv), pack_bf16x2(acc[h].z * inv, acc[h].w * inv));
+      *reinterpret_cast<uint2*>(out + h * kHeadDim + 4 * lane) = pk;
+      if (lse != nullptr && lane == 0) lse[h] = (mmax[h] + log2f(L[h])) * 0.69314718055994531f;
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kAWarps * 32, 1)
-sparse_attn_decode_partial_kernel(const __nv_bfloat16* __restrict__ q,
-                                  const __nv_bfloat16* __restrict__ k,
-                                  const __nv_bfloat16* __restrict__ v, int64_t L_cap,
-                                  const int64_t* __restrict__ cache_len,
-                                  const int32_t* __restrict__ idx, const int32_t* __restrict__ count,
-                                  int64_t B, int Hq, int Hkv, int r, int k_b, int n_split,
-                                  float scale, float* __restrict__ part_o, float* __restrict__ part_ml) {
+sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                          const __nv_bfloat16* __restrict__ v, int64_t L_cap,
+                          const int64_t* __restrict__ cache_len, const int32_t* __restrict__ idx,
+                          const int32_t* __restrict__ count, int64_t B, int Hq, int Hkv, int r, int k_b,
+                          int n_split, int split_len, float scale, float* __restrict__ part_o,
+                          float* __restrict__ part_ml, int* __restrict__ unit_done,
+                          __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   extern __shared__ __align__(128) uint8_t attn_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
   uint8_t* const wbuf = attn_smem + warp * kAWarpBytes;
@@ -311,108 +364,71 @@ sparse_attn_decode_partial_kernel(const __nv_bfloat16* __restrict__ q,
     const int g = (int)((wi / n_hc) % Hkv);
     const int64_t bb = wi / (n_hc * Hkv);
     const int64_t i = cache_len[bb] - 1;
-    float* po = part_o + (wi * n_split + split) * (8 * kHeadDim);
-    float* pml = part_ml + (wi * n_split + split) * 16;
-    if (i < 0 || i >= L_cap) {  // cache length outside [1, L_cap]: empty split, report
-      if (lane == 0 && split == 0) flag_device_error(kDevErrPosition);
-      if (lane < 8) { pml[lane] = -INFINITY; pml[8 + lane] = 0.f; }
-      continue;
-    }
-    const AttnRow a = make_row(i, r, idx + bb * (int64_t)k_b, count[bb], k_b);
     const int qh0 = g * group + 8 * hc;
     const int n_heads = min(8, group - 8 * hc);
-    const int s_beg = split * kDecodeSplit;
-    const int s_end = min(a.n_tok, s_beg + kDecodeSplit);
-    if (s_beg >= s_end) {  // empty split: contributes nothing
+    float* po = part_o + (wi * n_split + split) * (8 * kHeadDim);
+    float* pml = part_ml + (wi * n_split + split) * 16;
+    bool empty = false;
+    AttnRow a{};
+    int s_beg = 0, s_end = 0;
+    if (i < 0 || i >= L_cap) {  // cache length outside [1, L_cap]: empty split, report
+      if (lane == 0 && split == 0) flag_device_error(kDevErrPosition);
+      empty = true;
+    } else {
+      a = make_row(i, r, idx + bb * (int64_t)k_b, count[bb], k_b);
+      s_beg = split * split_len;
+      s_end = min(a.n_tok, s_beg + split_len);
+      empty = s_beg >= s_end;  // an empty split contributes nothing
+    }
+    if (empty) {
       if (lane < 8) { pml[lane] = -INFINITY; pml[8 + lane] = 0.f; }
-      continue;
+    } else {
+      const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
+      const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
+      float o[8][4], m2[2], l[2];
+      attend_slots(q + (bb * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end, scale * kLog2e, ring, o,
+                   m2, l);
+      float* st = reinterpret_cast<float*>(wbuf);
+      stage_o(st, o, 1.f, 1.f);
+      for (int h = 0; h < 8; ++h) {
+        const float4 x = *reinterpret_cast<const float4*>(st + h * kHeadDim + 4 * lane);
+        *reinterpret_cast<float4*>(po + h * kHeadDim + 4 * lane) = x;
+      }
+      if (gid == 0) {
+        pml[2 * t] = m2[0]; pml[2 * t + 1] = m2[1];
+        pml[8 + 2 * t] = l[0]; pml[8 + 2 * t + 1] = l[1];
+      }
     }
-    const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
-    const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
-    float o[8][4], m2[2], l[2];
-    attend_slots(q + (bb * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end, scale * kLog2e, ring, o,
-                 m2, l);
-    float* st = reinterpret_cast<float*>(wbuf);
-    stage_o(st, o, 1.f, 1.f);
-    for (int h = 0; h < 8; ++h) {
-      const float4 x = *reinterpret_cast<const float4*>(st + h * kHeadDim + 4 * lane);
-      *reinterpret_cast<float4*>(po + h * kHeadDim + 4 * lane) = x;
-    }
-    if (gid == 0) {
-      pml[2 * t] = m2[0]; pml[2 * t + 1] = m2[1];
-      pml[8 + 2 * t] = l[0]; pml[8 + 2 * t + 1] = l[1];
+    // Publish the partial, then count it; the last of the unit's splits combines.
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&unit_done[wi], 1) == n_split - 1;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      combine_unit(part_o + wi * n_split * (8 * kHeadDim), part_ml + wi * n_split * 16, n_split, n_heads,
+                   out + (bb * Hq + qh0) * kHeadDim, lse != nullptr ? lse + bb * Hq + qh0 : nullptr);
+      if (lane == 0) unit_done[wi] = 0;
     }
     __syncwarp();
   }
 }
 
-// Combine the splits of one (sequence, kv head, head chunk): 8 heads x 128 dims,
-// one warp per head.  Lanes hold the splits' maxima and sums (32 at a time),
-// so the weights come from warp reductions; the partial rows are then read with
-// independent loads (4 dims per lane).
-__global__ void __launch_bounds__(256)
-sparse_attn_decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                                  int64_t B, int Hq, int Hkv, int n_split,
-                                  __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  const int group = Hq / Hkv;
-  const int n_hc = (group + 7) / 8;
-  const int64_t wi = blockIdx.x;
-  const int hc = (int)(wi % n_hc);
-  const int g = (int)((wi / n_hc) % Hkv);
-  const int64_t bb = wi / (n_hc * Hkv);
-  const int qh0 = g * group + 8 * hc;
-  const int n_heads = min(8, group - 8 * hc);
-  const int h = threadIdx.x >> 5;  // 8 warps: one head each
-  const int lane = threadIdx.x & 31;
-  if (h >= n_heads) return;
-  const float* ml = part_ml + wi * n_split * 16;
-  float mmax = -INFINITY;
-  for (int s0 = 0; s0 < n_split; s0 += 32) {
-    float m = s0 + lane < n_split ? __ldg(ml + (s0 + lane) * 16 + h) : -INFINITY;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    mmax = fmaxf(mmax, m);
-  }
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < n_split; s0 += 32) {
-    const int sl = s0 + lane;
-    float w = 0.f, wl = 0.f;
-    if (sl < n_split) {
-      const float ms = __ldg(ml + sl * 16 + h);
-      if (ms > -INFINITY) {
-        w = exp2f(ms - mmax);
-        wl = w * __ldg(ml + sl * 16 + 8 + h);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
-    L += wl;
-    const int nn = min(32, n_split - s0);
-#pragma unroll 4
-    for (int j = 0; j < nn; ++j) {
-      const float wj = __shfl_sync(0xffffffffu, w, j);
-      if (wj != 0.f) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(part_o + ((wi * n_split + s0 + j) * 8 + h) * kHeadDim) + lane);
-        acc.x += wj * x.x; acc.y += wj * x.y; acc.z += wj * x.z; acc.w += wj * x.w;
-      }
-    }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;  // L = 0 only for a rejected cache length
-  const uint2 pk = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-  *reinterpret_cast<uint2*>(out + (bb * Hq + qh0 + h) * kHeadDim + 4 * lane) = pk;
-  if (lse != nullptr && lane == 0) lse[bb * Hq + qh0 + h] = (mmax + log2f(L)) * 0.69314718055994531f;
-}
-
-int decode_num_splits(int k_b, int r) {
+// Most splits a (sequence, kv head, head chunk) can use: splits of at least
+// kDecodeMinSplit slots over the longest token set, k_b r + r - 1.
+int decode_max_splits(int k_b, int r) {
   const int max_tok = k_b * r + r - 1;
-  return (max_tok + kDecodeSplit - 1) / kDecodeSplit;
+  return (max_tok + kDecodeMinSplit - 1) / kDecodeMinSplit;
 }
 
+// Partials (fp32 O of 8 heads, then max and sum per head) of every split, and
+// one completion counter per unit.
 size_t decode_workspace_bytes(int64_t B, int Hq, int Hkv, int k_b, int r) {
   const int n_hc = (Hq / Hkv + 7) / 8;
-  const int64_t units = B * Hkv * n_hc * (int64_t)decode_num_splits(k_b, r);
-  return (size_t)units * (8 * kHeadDim + 16) * sizeof(float);
+  const int64_t units = B * Hkv * n_hc;
+  const size_t parts = (size_t)units * decode_max_splits(k_b, r) * (8 * kHeadDim + 16) * sizeof(float);
+  return (parts + 255) / 256 * 256 + (size_t)units * sizeof(int);
 }
 
 // Grid of a persistent attention kernel (<= one CTA per SM); sets the kernel's
@@ -457,21 +473,36 @@ cudaError_t launch_sparse_attn_decode(const __nv_bfloat16* q, const __nv_bfloat1
                                       int k_b, float scale, __nv_bfloat16* out, float* lse,
                                       void* ws, cudaStream_t st) {
   const int n_hc = (Hq / Hkv + 7) / 8;
-  const int n_split = decode_num_splits(k_b, r);
   const int64_t units = B * Hkv * n_hc;
   if (units == 0) return cudaSuccess;
+  const int max_split = decode_max_splits(k_b, r);
   float* part_o = reinterpret_cast<float*>(ws);
-  float* part_ml = part_o + units * n_split * 8 * kHeadDim;
-  const int64_t items = units * n_split;
+  float* part_ml = part_o + units * max_split * 8 * kHeadDim;
+  const size_t parts = (size_t)units * max_split * (8 * kHeadDim + 16) * sizeof(float);
+  int* unit_done = reinterpret_cast<int*>(static_cast<char*>(ws) + (parts + 255) / 256 * 256);
+  cudaError_t e = cudaMemsetAsync(unit_done, 0, (size_t)units * sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  // As many splits per unit as fill the resident warps once (at least one,
+  // at most max_split), each a whole number of 16-slot groups.
   int grid = 0;
-  cudaError_t e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_partial_kernel), 1, items, &grid);
+  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), 1, units * max_split, &grid);
   if (e != cudaSuccess) return e;
-  sparse_attn_decode_partial_kernel<<<grid, kAWarps * 32, kASmemBytes, st>>>(
-      q, k, v, L_cap, cache_len, idx, count, B, Hq, Hkv, r, k_b, n_split, scale, part_o, part_ml);
-  e = count_launch(cudaGetLastError());
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  sparse_attn_decode_combine_kernel<<<(unsigned)units, 256, 0, st>>>(part_o, part_ml, B, Hq, Hkv,
-                                                                     n_split, out, lse);
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  int64_t n_split = (int64_t)sms * kAWarps / units;
+  n_split = n_split < 1 ? 1 : (n_split > max_split ? max_split : n_split);
+  const int max_tok = k_b * r + r - 1;
+  int split_len = (int)((max_tok + n_split - 1) / n_split);
+  split_len = (split_len + kAGroup - 1) / kAGroup * kAGroup;
+  n_split = (max_tok + split_len - 1) / split_len;
+  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), 1, units * n_split, &grid);
+  if (e != cudaSuccess) return e;
+  sparse_attn_decode_kernel<<<grid, kAWarps * 32, kASmemBytes, st>>>(
+      q, k, v, L_cap, cache_len, idx, count, B, Hq, Hkv, r, k_b, (int)n_split, split_len, scale, part_o, part_ml,
+      unit_done, out, lse);
   return count_launch(cudaGetLastError());
 }
 

@@ -13,6 +13,8 @@
 // that bin holds exactly the number needed, or when it is a single value (an
 // exact tie, resolved by taking the lowest block ids first).  A final ordered
 // compaction writes the winners in ascending block order.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace qsa {
@@ -216,6 +218,93 @@ struct SelectFastSmem {
   int32_t cb[kSelCand];
 };
 
+// Refinement and ordered emission on a candidate copy: sm.cu / sm.cb hold, in
+// block order, the ncand entries whose pattern is >= lo; `need` of those in
+// [lo, hi] win besides every entry above hi.
+__device__ void select_from_candidates(SelectFastSmem& sm, int ncand, uint32_t lo, uint32_t hi, int need, int k_b,
+                                       int32_t* __restrict__ out) {
+  const int base_bin = (kSelThreads - 1 - threadIdx.x) * kSelBinsPerThread;
+  int loc[kSelBinsPerThread];
+  int sum = 0;
+  // Refine [lo, hi] on the copy (entries > hi are all winners).
+  int done = 0;
+  for (int guard = 0; !done && guard < 6; ++guard) {
+    const uint32_t width = hi - lo;
+    const int nbits = 32 - __clz(width);
+    const int shift = nbits > 11 ? nbits - 11 : 0;
+    for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) sm.base.hist[j] = 0;
+    __syncthreads();
+    for (int e = threadIdx.x; e < ncand; e += kSelThreads) {
+      const uint32_t u = sm.cu[e];
+      if (u >= lo && u <= hi) atomicAdd(&sm.base.hist[(u - lo) >> shift], 1);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < kSelBinsPerThread; ++q) loc[q] = sm.base.hist[base_bin + kSelBinsPerThread - 1 - q];
+    sum = loc[0] + loc[1] + loc[2] + loc[3];
+    const int ab0 = block_exclusive_scan(sum, sm.base.warp_sums, &sm.base.total);
+    if (ab0 < need && ab0 + sum >= need) {
+      int above = ab0;
+#pragma unroll
+      for (int q = 0; q < kSelBinsPerThread; ++q) {
+        if (above + loc[q] >= need) {
+          const int bin = base_bin + kSelBinsPerThread - 1 - q;
+          const uint32_t nlo = lo + ((uint32_t)bin << shift);
+          const uint32_t span = (1u << shift) - 1u;
+          const uint32_t nhi = (hi - nlo) < span ? hi : nlo + span;
+          const int nneed = need - above;
+          sm.base.lo = nlo;
+          sm.base.hi = nhi;
+          sm.base.need = nneed;
+          sm.base.done = (loc[q] == nneed) ? 1 : (nlo == nhi ? 2 : 0);
+          break;
+        }
+        above += loc[q];
+      }
+    }
+    __syncthreads();
+    lo = sm.base.lo;
+    hi = sm.base.hi;
+    need = sm.base.need;
+    done = sm.base.done;
+    __syncthreads();
+  }
+  // Ordered emission from the copy (already in block order).
+  int wr = 0, ties_taken = 0;
+  for (int e0 = 0; e0 < ncand; e0 += 4 * kSelThreads) {
+    const int e = e0 + 4 * threadIdx.x;
+    uint32_t win = 0, tie = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (e + q < ncand) {
+        const uint32_t u = sm.cu[e + q];
+        if (u > hi || (done == 1 && u >= lo)) win |= 1u << q;
+        else if (done == 2 && u == lo) tie |= 1u << q;
+      }
+    }
+    const int tie_before = ties_taken + block_exclusive_scan(__popc(tie), sm.base.warp_sums, &sm.base.total);
+    const int tie_total = sm.base.total;
+#pragma unroll
+    for (int q = 0, k = 0; q < 4; ++q) {
+      if (tie & (1u << q)) {
+        if (tie_before + k < need) win |= 1u << q;
+        ++k;
+      }
+    }
+    ties_taken += tie_total;
+    const int before = wr + block_exclusive_scan(__popc(win), sm.base.warp_sums, &sm.base.total);
+    const int wtot = sm.base.total;
+#pragma unroll
+    for (int q = 0, k = 0; q < 4; ++q) {
+      if (win & (1u << q)) {
+        if (before + k < k_b) out[before + k] = sm.cb[e + q];
+        ++k;
+      }
+    }
+    wr += wtot;
+  }
+}
+
 __device__ void cta_select_row_fast(const float* __restrict__ s, int64_t c, int k_b, int32_t* __restrict__ out,
                                     SelectFastSmem& sm) {
   // Pass 1: bins of the top 11 bits of the pattern.
@@ -296,83 +385,7 @@ __device__ void cta_select_row_fast(const float* __restrict__ s, int64_t c, int 
     written += tot;
   }
   __syncthreads();
-  // Refine [lo, hi] on the copy (entries > hi are all winners).
-  int done = 0;
-  for (int guard = 0; !done && guard < 6; ++guard) {
-    const uint32_t width = hi - lo;
-    const int nbits = 32 - __clz(width);
-    const int shift = nbits > 11 ? nbits - 11 : 0;
-    for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) sm.base.hist[j] = 0;
-    __syncthreads();
-    for (int e = threadIdx.x; e < ncand; e += kSelThreads) {
-      const uint32_t u = sm.cu[e];
-      if (u >= lo && u <= hi) atomicAdd(&sm.base.hist[(u - lo) >> shift], 1);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int q = 0; q < kSelBinsPerThread; ++q) loc[q] = sm.base.hist[base_bin + kSelBinsPerThread - 1 - q];
-    sum = loc[0] + loc[1] + loc[2] + loc[3];
-    const int ab0 = block_exclusive_scan(sum, sm.base.warp_sums, &sm.base.total);
-    if (ab0 < need && ab0 + sum >= need) {
-      int above = ab0;
-#pragma unroll
-      for (int q = 0; q < kSelBinsPerThread; ++q) {
-        if (above + loc[q] >= need) {
-          const int bin = base_bin + kSelBinsPerThread - 1 - q;
-          const uint32_t nlo = lo + ((uint32_t)bin << shift);
-          const uint32_t span = (1u << shift) - 1u;
-          const uint32_t nhi = (hi - nlo) < span ? hi : nlo + span;
-          const int nneed = need - above;
-          sm.base.lo = nlo;
-          sm.base.hi = nhi;
-          sm.base.need = nneed;
-          sm.base.done = (loc[q] == nneed) ? 1 : (nlo == nhi ? 2 : 0);
-          break;
-        }
-        above += loc[q];
-      }
-    }
-    __syncthreads();
-    lo = sm.base.lo;
-    hi = sm.base.hi;
-    need = sm.base.need;
-    done = sm.base.done;
-    __syncthreads();
-  }
-  // Ordered emission from the copy (already in block order).
-  int wr = 0, ties_taken = 0;
-  for (int e0 = 0; e0 < ncand; e0 += 4 * kSelThreads) {
-    const int e = e0 + 4 * threadIdx.x;
-    uint32_t win = 0, tie = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (e + q < ncand) {
-        const uint32_t u = sm.cu[e + q];
-        if (u > hi || (done == 1 && u >= lo)) win |= 1u << q;
-        else if (done == 2 && u == lo) tie |= 1u << q;
-      }
-    }
-    const int tie_before = ties_taken + block_exclusive_scan(__popc(tie), sm.base.warp_sums, &sm.base.total);
-    const int tie_total = sm.base.total;
-#pragma unroll
-    for (int q = 0, k = 0; q < 4; ++q) {
-      if (tie & (1u << q)) {
-        if (tie_before + k < need) win |= 1u << q;
-        ++k;
-      }
-    }
-    ties_taken += tie_total;
-    const int before = wr + block_exclusive_scan(__popc(win), sm.base.warp_sums, &sm.base.total);
-    const int wtot = sm.base.total;
-#pragma unroll
-    for (int q = 0, k = 0; q < 4; ++q) {
-      if (win & (1u << q)) {
-        if (before + k < k_b) out[before + k] = sm.cb[e + q];
-        ++k;
-      }
-    }
-    wr += wtot;
-  }
+  select_from_candidates(sm, ncand, lo, hi, need, k_b, out);
 }
 
 // One CTA per row; rows with c <= k_b keep every block.
@@ -394,6 +407,166 @@ topk_select_fast_kernel(const float* __restrict__ S, int64_t s_stride, const int
   }
   cta_select_row_fast(S + (int64_t)blockIdx.x * s_stride, c, k_b, out, sm);
   if (threadIdx.x == 0) count[row] = k_b;
+}
+
+// ---------------------------------------------------------------------------------------------
+// The same selection with each row split over a cluster of kSelCluster CTAs
+// (decode: few rows, long rows).  Every CTA takes a quarter of the row: local
+// histograms of the top 11 bits, merged by every CTA through distributed
+// shared memory; ordered copies of the entries at or above the boundary bin,
+// gathered into the first CTA's candidate arrays in rank (= block) order; that
+// CTA refines and emits.
+constexpr int kSelCluster = 4;
+
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
+topk_select_cluster_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t* __restrict__ q_pos,
+                           int64_t n_q, int64_t row_lo, int r, int k_b, int64_t c_cap,
+                           int32_t* __restrict__ idx, int32_t* __restrict__ count) {
+  namespace cg = cooperative_groups;
+  __shared__ SelectFastSmem sm;
+  __shared__ int n_local;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int64_t lrow = blockIdx.x / kSelCluster;
+  const int64_t row = row_lo + lrow;
+  const int64_t bb = row / n_q;
+  const int64_t pos = q_pos[bb] + row % n_q;
+  int64_t c = (pos + 1) / r;
+  if (c > c_cap) c = c_cap;
+  int32_t* out = idx + row * (int64_t)k_b;
+  if (c <= k_b) {  // the same for the whole cluster: nobody touches another CTA's memory
+    if (rank == 0) {
+      for (int j = threadIdx.x; j < k_b; j += kSelThreads) out[j] = j < c ? j : -1;
+      if (threadIdx.x == 0) count[row] = (int32_t)c;
+    }
+    return;
+  }
+  const float* s = S + lrow * s_stride;
+  // This CTA's part of the row, in batches of kSelThreads x 32 scores; thread
+  // t owns the 32 consecutive scores at 32 t of each batch (8 float4 loads in
+  // flight, one line per thread).
+  const int64_t part = ((c + 32 * kSelCluster - 1) / (32 * kSelCluster)) * 32;
+  const int64_t e_lo = c < rank * part ? c : rank * part;
+  const int64_t e_hi = c < e_lo + part ? c : e_lo + part;
+  auto load_batch = [&](int64_t b0, uint32_t (&u)[32]) {
+    const int64_t e = b0 + 32 * (int64_t)threadIdx.x;
+    if (e + 32 <= e_hi) {
+      float4 x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = reinterpret_cast<const float4*>(s + e)[j];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        u[4 * j] = score_key(x[j].x); u[4 * j + 1] = score_key(x[j].y);
+        u[4 * j + 2] = score_key(x[j].z); u[4 * j + 3] = score_key(x[j].w);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) u[j] = e + j < e_hi ? score_key(s[e + j]) : 0xffffffffu;  // past the end: no bin
+    }
+  };
+  // Pass 1: local histogram of this CTA's part.
+  for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) sm.base.hist[j] = 0;
+  __syncthreads();
+  for (int64_t b0 = e_lo; b0 < e_hi; b0 += 32 * kSelThreads) {
+    uint32_t u[32];
+    load_batch(b0, u);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (u[j] != 0xffffffffu) atomicAdd(&sm.base.hist[u[j] >> 20], 1);
+  }
+  cluster.sync();
+  // Merged histogram: this thread's 4 bins summed over the cluster.
+  const int base_bin = (kSelThreads - 1 - threadIdx.x) * kSelBinsPerThread;
+  int loc[kSelBinsPerThread] = {0, 0, 0, 0};
+  for (int q = 0; q < kSelCluster; ++q) {
+    const int* h = cluster.map_shared_rank(sm.base.hist, q);
+#pragma unroll
+    for (int j = 0; j < kSelBinsPerThread; ++j) loc[j] += h[base_bin + kSelBinsPerThread - 1 - j];
+  }
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < kSelBinsPerThread; ++j) sum += loc[j];
+  const int above0 = block_exclusive_scan(sum, sm.base.warp_sums, &sm.base.total);
+  if (above0 < k_b && above0 + sum >= k_b) {
+    int above = above0;
+#pragma unroll
+    for (int j = 0; j < kSelBinsPerThread; ++j) {
+      if (above + loc[j] >= k_b) {
+        const int bin = base_bin + kSelBinsPerThread - 1 - j;
+        sm.base.lo = (uint32_t)bin << 20;
+        sm.base.hi = ((uint32_t)bin << 20) | 0xfffffu;
+        sm.base.need = k_b - above;
+        sm.base.done = above + loc[j];  // entries at or above the bin, whole row
+        break;
+      }
+      above += loc[j];
+    }
+  }
+  cluster.sync();  // every CTA has read the others' histograms
+  const uint32_t lo = sm.base.lo, hi = sm.base.hi;
+  const int need = sm.base.need;
+  const int ncand = sm.base.done;
+  if (ncand > kSelCand) {  // boundary bin too full for the copy: the first CTA takes the whole row
+    if (rank == 0) {
+      __syncthreads();
+      cta_select_row(s, c, k_b, out, sm.base);
+      if (threadIdx.x == 0) count[row] = k_b;
+    }
+    return;
+  }
+  // Pass 2: ordered copy of this part's entries with pattern >= lo.
+  int written = 0;
+  for (int64_t b0 = e_lo; b0 < e_hi; b0 += 32 * kSelThreads) {
+    uint32_t u[32], take = 0;
+    load_batch(b0, u);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (u[j] != 0xffffffffu && u[j] >= lo) take |= 1u << j;
+    const int before = written + block_exclusive_scan(__popc(take), sm.base.warp_sums, &sm.base.total);
+    const int tot = sm.base.total;
+    const int64_t e = b0 + 32 * (int64_t)threadIdx.x;
+    int k = before;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if ((take >> j) & 1u) {
+        if (k < kSelCand) {
+          sm.cu[k] = u[j];
+          sm.cb[k] = (int32_t)(e + j);
+        }
+        ++k;
+      }
+    }
+    written += tot;
+  }
+  if (threadIdx.x == 0) n_local = written;
+  cluster.sync();
+  // Append this part's candidates to the first CTA's arrays after the lower ranks'.
+  int offset = 0;
+  for (int q = 0; q < rank; ++q) offset += *cluster.map_shared_rank(&n_local, q);
+  if (rank > 0) {
+    uint32_t* du = cluster.map_shared_rank(sm.cu, 0);
+    int32_t* db = cluster.map_shared_rank(sm.cb, 0);
+    const int n_mine = min(written, kSelCand);
+    for (int j = threadIdx.x; j < n_mine; j += kSelThreads) {
+      if (offset + j < kSelCand) {
+        du[offset + j] = sm.cu[j];
+        db[offset + j] = sm.cb[j];
+      }
+    }
+  }
+  cluster.sync();  // the first CTA's arrays are complete; the others are done
+  if (rank != 0) return;
+  select_from_candidates(sm, ncand, lo, hi, need, k_b, out);
+  if (threadIdx.x == 0) count[row] = k_b;
+}
+
+cudaError_t launch_topk_select_cluster(const float* S, int64_t s_stride, const int64_t* q_pos, int64_t n_q,
+                                       int64_t row_lo, int64_t n_rows, int r, int k_b, int64_t c_cap,
+                                       int32_t* idx, int32_t* count, cudaStream_t st) {
+  if (n_rows <= 0) return cudaSuccess;
+  topk_select_cluster_kernel<<<(unsigned)(n_rows * kSelCluster), kSelThreads, 0, st>>>(
+      S, s_stride, q_pos, n_q, row_lo, r, k_b, c_cap, idx, count);
+  return count_launch(cudaGetLastError());
 }
 
 cudaError_t launch_topk_select_fast(const float* S, int64_t s_stride, const int64_t* q_pos, int64_t n_q,
