@@ -51,13 +51,14 @@
 
 namespace qsa {
 
-constexpr int kTT = 64;                  // query tokens per tile
-constexpr int kNRows = kTT * kIdxHeads;  // 256: MMA N (token, head rows)
+constexpr int kTT = 48;                  // query tokens per tile
+constexpr int kNRows = kTT * kIdxHeads;  // 192: MMA N (token, head rows)
 constexpr int kMB = 128;                 // blocks per chunk: MMA M
-constexpr int kAStages = 2;              // kbar TMA ring depth
-constexpr int kEpiWarps = 16;            // 4 per TMEM lane quarter
-constexpr int kFThreads = 32 * (2 + kEpiWarps);              // 576
-constexpr uint32_t kTmemCols = 2 * kNRows;                   // 512: two accumulators
+constexpr int kAStages = 3;              // kbar TMA ring depth
+constexpr int kEpiWarps = 12;            // 3 per TMEM lane quarter, 16 tokens each
+constexpr int kFThreads = 32 * (2 + kEpiWarps);              // 448: 128 registers per thread
+constexpr uint32_t kAccCols = 256;                           // TMEM columns between the two accumulators
+constexpr uint32_t kTmemCols = 2 * kAccCols;                 // 512
 constexpr int kPBins = 512;              // pilot bins (1/16 octave), packed 2 per word
 constexpr int kPShift = 19;              // bits below the bin index
 constexpr int kPBase = 1920;             // (bits of 2^-7) >> 19: bins of 2 x score start at 2^-7
@@ -72,7 +73,7 @@ constexpr int kFbCtas = 148;             // fallback kernel CTAs (one row each a
 constexpr int kTilesPerLaunch = 1024;    // tiles per fused launch (bounds the row buffers: 3 GiB)
 constexpr int kFinKWarps = 4;            // warps per CTA of the finalize kernel
 constexpr uint32_t kABytes = kMB * 128 * 2;     // 32 KB
-constexpr uint32_t kBBytes = kNRows * 128 * 2;  // 64 KB
+constexpr uint32_t kBBytes = kNRows * 128 * 2;  // 48 KB
 
 // Optional per-role cycle counters for tuning builds (-DQSA_FUSED_PROF).
 #ifdef QSA_FUSED_PROF
@@ -510,7 +511,7 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           FPROF_ADD(3, t2);
           tc_fence_after();
           const uint32_t a0 = smem_u32(S.a[st][0]), a1 = smem_u32(S.a[st][1]);
-          const uint32_t d = tmem + (uint32_t)(acc * kNRows);
+          const uint32_t d = tmem + (uint32_t)acc * kAccCols;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t aoff = (kk < 4 ? a0 : a1) + (uint32_t)((kk & 3) * 32);
@@ -544,20 +545,25 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       const int cmin16 = min((pos16 + 1) >> rshift, cap32);  // smallest c of the warp's tokens
       // Segment of (token 16 h + j, this warp's lane quarter): seg0 + j * 4 kSeg.
       uint2* const seg0 = buf + ((lt * kTT + 16 * h) * 4 + q4) * kSeg;
-      // Entry count of token 16 h + lane, held by lanes 0-15.
-      int my_cnt = 0;
+      // Thresholds and entry counts of the warp's 16 tokens (the same in every lane).
+      uint32_t tau16[16];
+      int cnt16[16];
+#pragma unroll
+      for (int k2 = 0; k2 < 16; ++k2) {
+        tau16[k2] = 0xffffffffu;
+        cnt16[k2] = 0;
+      }
       const int total = m.npilot + m.nchunks;
       for (int x = 0; x < total; ++x, ++ct) {
         const bool pilot = x < m.npilot;
         if (x == m.npilot) {
-          // ---- pilot done: thresholds of tokens ew, ew + 16, ew + 32, ew + 48
+          // ---- pilot done: thresholds of tokens ew, ew + kEpiWarps, ...
           FPROF_T0(tt0);
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.pilot_bar);
           if (!warp_wait(&S.pilot_bar, pilot_n & 1, abort_flag)) { ok = false; break; }
 #pragma unroll 1
-          for (int j = 0; j < kTT / 16; ++j) {
-            const int t = ew + 16 * j;
+          for (int t = ew; t < kTT; t += kEpiWarps) {
             const int64_t c = token_c(m, t, rshift, c_cap);
             // Rows that do not select (past the end, or c <= k_B) collect nothing.
             const uint32_t tau = pilot_tau(S.phist[t], c, k_b);
@@ -566,6 +572,14 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.tau_bar);
           if (!warp_wait(&S.tau_bar, pilot_n & 1, abort_flag)) { ok = false; break; }
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const uint4 t4 = *reinterpret_cast<const uint4*>(&S.tau[16 * h + 4 * k4]);
+            tau16[4 * k4] = t4.x;
+            tau16[4 * k4 + 1] = t4.y;
+            tau16[4 * k4 + 2] = t4.z;
+            tau16[4 * k4 + 3] = t4.w;
+          }
           if (ew == 0 && lane == 0) FPROF_ADD(8, tt0);
           ++pilot_n;
         }
@@ -584,7 +598,7 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         uint32_t u16[16];
         FPROF_T0(tl);
         {
-          const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(acc * kNRows + 64 * h);
+          const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)acc * kAccCols + (uint32_t)(64 * h);
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
             uint32_t v[32];
@@ -614,53 +628,53 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         // below the first token's visible range.
         const int warp_last = pilot ? (m.mc * kMB) * kPilotStride : gbase + 32;
         const bool chunk_all_visible = warp_last <= cmin16;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const uint32_t* const uu = &u16[8 * g];
-          const int tg = 16 * h + 8 * g;  // first token of the group
-          // Lanes (blocks) each of the 8 tokens sees: a prefix of the warp, as
-          // block ids grow with the lane.  Tokens that do not select are excluded
-          // by their threshold; their pilot counts are never read.
-          auto vis_mask = [&](int kk) -> unsigned {
-            if (chunk_all_visible) return 0xffffffffu;
-            int c = (pos16 + 8 * g + kk + 1) >> rshift;
-            c = c < cap32 ? c : cap32;
-            int lim;
-            if (pilot) {
-              const int ng = c > ph ? (c - ph + kPilotStride - 1) / kPilotStride : 0;
-              lim = (ng < m.ngroups ? ng : m.ngroups) - gbase;
-            } else {
-              lim = c - gbase;
-            }
-            return lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
-          };
+        // Lanes (blocks) token 16 h + k2 sees: a prefix of the warp, as block
+        // ids grow with the lane.  Tokens that do not select are excluded by
+        // their threshold; their pilot counts are never read.
+        auto vis_mask = [&](int k2) -> unsigned {
+          if (chunk_all_visible) return 0xffffffffu;
+          int c = (pos16 + k2 + 1) >> rshift;
+          c = c < cap32 ? c : cap32;
+          int lim;
           if (pilot) {
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              int bin = (int)(uu[kk] >> kPShift) - kPBase;
-              bin = bin < 0 ? 0 : (bin > kPBins - 1 ? kPBins - 1 : bin);
-              if ((vis_mask(kk) >> lane) & 1u) atomicAdd(&S.phist[tg + kk][bin >> 1], (bin & 1) ? 65536u : 1u);
-            }
+            const int ng = c > ph ? (c - ph + kPilotStride - 1) / kPilotStride : 0;
+            lim = (ng < m.ngroups ? ng : m.ngroups) - gbase;
           } else {
-            const uint4 ta = *reinterpret_cast<const uint4*>(&S.tau[tg]);
-            const uint4 tb4 = *reinterpret_cast<const uint4*>(&S.tau[tg + 4]);
-            const uint32_t tauv[8] = {ta.x, ta.y, ta.z, ta.w, tb4.x, tb4.y, tb4.z, tb4.w};
-            bool pass = false;
+            lim = c - gbase;
+          }
+          return lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
+        };
+        if (pilot) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) pass |= uu[kk] >= tauv[kk];
-            if (__any_sync(0xffffffffu, pass)) {  // a chunk whose 256 pairs all fall below tau is skipped
-              if (ew == 0 && lane == 0) FPROF_CNT(2, 1);
-              const unsigned lt_mask = (1u << lane) - 1u;
-              int add = 0;
+          for (int k2 = 0; k2 < 16; ++k2) {
+            int bin = (int)(u16[k2] >> kPShift) - kPBase;
+            bin = bin < 0 ? 0 : (bin > kPBins - 1 ? kPBins - 1 : bin);
+            if ((vis_mask(k2) >> lane) & 1u) atomicAdd(&S.phist[16 * h + k2][bin >> 1], (bin & 1) ? 65536u : 1u);
+          }
+        } else {
+          bool pass = false;
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const unsigned tmk = __ballot_sync(0xffffffffu, uu[kk] >= tauv[kk]) & vis_mask(kk);
-                const int pos = __shfl_sync(0xffffffffu, my_cnt, 8 * g + kk) + __popc(tmk & lt_mask);
-                if (((tmk >> lane) & 1u) && pos < kSeg)
-                  seg0[(8 * g + kk) * 4 * kSeg + pos] = make_uint2(uu[kk], (uint32_t)bi);
-                add = lane == 8 * g + kk ? __popc(tmk) : add;
+          for (int k2 = 0; k2 < 16; ++k2) pass |= u16[k2] >= tau16[k2];
+          if (__any_sync(0xffffffffu, pass)) {  // a chunk whose 512 pairs all fall below tau is skipped
+            if (ew == 0 && lane == 0) FPROF_CNT(2, 1);
+            const unsigned lt_mask = (1u << lane) - 1u;
+            if (chunk_all_visible) {
+#pragma unroll
+              for (int k2 = 0; k2 < 16; ++k2) {
+                const bool mine = u16[k2] >= tau16[k2];
+                const unsigned tmk = __ballot_sync(0xffffffffu, mine);
+                const int pos = cnt16[k2] + __popc(tmk & lt_mask);
+                if (mine && pos < kSeg) seg0[k2 * 4 * kSeg + pos] = make_uint2(u16[k2], (uint32_t)bi);
+                cnt16[k2] += __popc(tmk);
               }
-              my_cnt += add;
+            } else {
+#pragma unroll
+              for (int k2 = 0; k2 < 16; ++k2) {
+                const unsigned tmk = __ballot_sync(0xffffffffu, u16[k2] >= tau16[k2]) & vis_mask(k2);
+                const int pos = cnt16[k2] + __popc(tmk & lt_mask);
+                if (((tmk >> lane) & 1u) && pos < kSeg) seg0[k2 * 4 * kSeg + pos] = make_uint2(u16[k2], (uint32_t)bi);
+                cnt16[k2] += __popc(tmk);
+              }
             }
           }
         }
@@ -668,7 +682,13 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       }
       if (!ok) break;
       // ---- tile done: this warp's entry counts go to the finalize kernel
-      if (lane < 16) cnt[(lt * 4 + q4) * kTT + 16 * h + lane] = my_cnt;
+      if (lane == 0) {
+        int4* const dst = reinterpret_cast<int4*>(cnt + (lt * 4 + q4) * kTT + 16 * h);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          dst[k4] = make_int4(cnt16[4 * k4], cnt16[4 * k4 + 1], cnt16[4 * k4 + 2], cnt16[4 * k4 + 3]);
+      }
+      __syncwarp();
     }
   }
 
