@@ -628,28 +628,28 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         // below the first token's visible range.
         const int warp_last = pilot ? (m.mc * kMB) * kPilotStride : gbase + 32;
         const bool chunk_all_visible = warp_last <= cmin16;
-        // Lanes (blocks) token 16 h + k2 sees: a prefix of the warp, as block
-        // ids grow with the lane.  Tokens that do not select are excluded by
-        // their threshold; their pilot counts are never read.
+        // Lanes (blocks) token 16 h + k2 sees in a main chunk: a prefix of the
+        // warp, as block ids grow with the lane.  Tokens that do not select are
+        // excluded by their threshold.
         auto vis_mask = [&](int k2) -> unsigned {
           if (chunk_all_visible) return 0xffffffffu;
           int c = (pos16 + k2 + 1) >> rshift;
           c = c < cap32 ? c : cap32;
-          int lim;
-          if (pilot) {
-            const int ng = c > ph ? (c - ph + kPilotStride - 1) / kPilotStride : 0;
-            lim = (ng < m.ngroups ? ng : m.ngroups) - gbase;
-          } else {
-            lim = c - gbase;
-          }
+          const int lim = c - gbase;
           return lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
         };
         if (pilot) {
+          // The sample is every sampled block the tile's last row sees: the
+          // visible ranges of the tile's rows differ by at most 12 blocks, and
+          // tau only sets the fraction of a row's scores to collect.  The
+          // collect pass applies each row's exact range.
+          if (gbase + lane < m.ngroups) {
 #pragma unroll
-          for (int k2 = 0; k2 < 16; ++k2) {
-            int bin = (int)(u16[k2] >> kPShift) - kPBase;
-            bin = bin < 0 ? 0 : (bin > kPBins - 1 ? kPBins - 1 : bin);
-            if ((vis_mask(k2) >> lane) & 1u) atomicAdd(&S.phist[16 * h + k2][bin >> 1], (bin & 1) ? 65536u : 1u);
+            for (int k2 = 0; k2 < 16; ++k2) {
+              int bin = (int)(u16[k2] >> kPShift) - kPBase;
+              bin = bin < 0 ? 0 : (bin > kPBins - 1 ? kPBins - 1 : bin);
+              atomicAdd(&S.phist[16 * h + k2][bin >> 1], (bin & 1) ? 65536u : 1u);
+            }
           }
         } else {
           bool pass = false;
