@@ -88,6 +88,69 @@ def decode_work(batch: int, cache_len: int, r: int, k_b: int, hq: int, hkv: int,
             "gather_bytes": batch * gather, "tokens": t}
 
 
+def decode_multi_work(batch: int, cache_len: int, next_n: int, r: int, k_b: int, hq: int, hkv: int,
+                      d: int = 128, h_idx: int = 4) -> dict:
+    """One multi-token decode step: the k-bar scan once per sequence (up to the
+    last row's visible blocks), a gather per row, and the rows' small tensors."""
+    c_last = cache_len // r
+    kbar_bytes = c_last * d * 2
+    gather = 0
+    for j in range(next_n):
+        i = cache_len - next_n + j
+        c = (i + 1) // r
+        gather += (min(c, k_b) * r + (i + 1 - c * r)) * hkv * 2 * d * 2
+    small = next_n * (h_idx * d * 2 + hq * d * 2 * 2 + k_b * 4)
+    return {"bytes": batch * (kbar_bytes + gather + small), "kbar_bytes": batch * kbar_bytes,
+            "gather_bytes": batch * gather}
+
+
+def multi_decode_measure(qsa, spec, steps: int, warmup: int, dev, hbm_gbs: float) -> dict:
+    """Times the multi-token decode step (the pages' decode mode: batch 4, next_n
+    = 4): qsa_index_topk for all rows of each sequence, then
+    qsa_sparse_attn_decode_multi.  CUDA events around each step, L2 flushed
+    between steps outside the events; the median step is reported."""
+    import torch
+    from block_sparse_long_17_b300.workloads import make_decode
+    wl = make_decode(spec, dev)
+    cfg = qsa.Config(r=spec.r, k_tokens=spec.k_tokens, rope_dims=spec.rope_dims, rope_base=spec.rope_base)
+    B, nn = spec.batch, spec.next_n
+    q_pos = wl["cache_lens"] - nn
+    idx = torch.empty((B, nn, cfg.k_b), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, nn), dtype=torch.int32, device=dev)
+    ws = torch.empty((qsa.qsa_index_topk_workspace(cfg, B, nn, wl["n_blocks"]),), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(wl["q"])
+    lse = torch.empty((B, nn, spec.hq), dtype=torch.float32, device=dev)
+    wsa = torch.empty((qsa.qsa_sparse_attn_decode_multi_workspace(cfg, B, nn, spec.hq, spec.hkv),),
+                      dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        qsa.qsa_index_topk(cfg, wl["q_idx"], wl["kbar"], q_pos, wl["n_blocks"], idx, cnt, ws)
+        qsa.qsa_sparse_attn_decode_multi(cfg, wl["q"], wl["k"], wl["v"], wl["cache_lens"], idx, cnt, out, wsa, lse)
+
+    for _ in range(max(warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(max(steps, 10)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    assert qsa.qsa_read_device_error() == 0
+    us = statistics.median(ts) * 1e3
+    wk = decode_multi_work(B, wl["cache_len"], nn, spec.r, spec.k_b, spec.hq, spec.hkv)
+    achieved = wk["bytes"] / (us * 1e-6) / 1e9
+    return {"workload": spec.name, "batch": B, "next_n": nn, "ctx_tokens": wl["cache_len"],
+            "us_per_step": us, "bytes_per_step": wk["bytes"],
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved / hbm_gbs}}
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -209,6 +272,8 @@ def main():
     ap.add_argument("--prefill-workload", default=PREFILL,
                     help="prefill workload name (smaller ones serve profiling runs)")
     ap.add_argument("--decode-workload", default=DECODE, help="decode workload name, or 'none'")
+    ap.add_argument("--multi-decode-workload", default="decode_1m_b4_next4",
+                    help="multi-token decode workload timed beside the main step, or 'none'")
     args = ap.parse_args()
 
     import torch
@@ -252,6 +317,14 @@ def main():
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream(dev)
+
+    # The multi-token decode step is a separate workload, timed first on a clean
+    # device and its buffers freed before the main step's are drawn.
+    decode_multi = None
+    if args.multi_decode_workload != "none":
+        decode_multi = multi_decode_measure(qsa, WORKLOADS[args.multi_decode_workload], args.steps, args.warmup,
+                                            dev, pk["hbm_gbs"])
+        torch.cuda.empty_cache()
 
     cfg = qsa.Config(r=pspec.r, k_tokens=pspec.k_tokens, rope_dims=pspec.rope_dims, rope_base=pspec.rope_base)
     wl = make_prefill(pspec, dev)
@@ -377,6 +450,8 @@ def main():
 
     if not do_decode:
         line["decode_us_per_step"] = None
+    if decode_multi is not None:
+        line["decode_multi"] = decode_multi
     if not args.no_e2e and rank == 0 and do_decode:
         line["e2e"] = e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev)
     if not args.no_cpu_baseline and rank == 0 and do_decode:

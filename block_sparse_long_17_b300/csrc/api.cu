@@ -162,9 +162,9 @@ qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* 
                                         n_q, n_blocks_max, r, k_b, idx, count, w + L.s_off, st));
   }
   const int64_t rows = B * n_q;
-  if (n_q == 1 && rows <= L.rows_per_launch) {  // decode: one query row per sequence
-    e = launch_decode_scan(qt, static_cast<const __nv_bfloat16*>(kbar), kbar_stride_b, q_pos, B, r, n_blocks_max,
-                           S, L.s_stride, st);
+  if (n_q <= kDecodeMaxRows && rows <= L.rows_per_launch) {  // decode: one or a few query rows per sequence
+    e = launch_decode_scan(qt, static_cast<const __nv_bfloat16*>(kbar), kbar_stride_b, q_pos, B, (int)n_q, r,
+                           n_blocks_max, S, L.s_stride, st);
     if (e != cudaSuccess) return from_cuda(e);
     return from_cuda(launch_topk_select_cluster(S, L.s_stride, q_pos, n_q, 0, rows, r, k_b, n_blocks_max, idx, count, st));
   }
@@ -221,7 +221,36 @@ qsa_status qsa_sparse_attn_decode(const qsa_config* cfg, const void* q, const vo
   if (ws_bytes < qsa_sparse_attn_decode_workspace(cfg, B, Hq, Hkv)) return QSA_ERR_WORKSPACE;
   return from_cuda(launch_sparse_attn_decode(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_cache),
-      static_cast<const __nv_bfloat16*>(v_cache), L_cap, cache_len, idx, count, B, Hq, Hkv,
+      static_cast<const __nv_bfloat16*>(v_cache), L_cap, cache_len, idx, count, B, 1, Hq, Hkv,
+      cfg->r, k_blocks(cfg), scale, static_cast<__nv_bfloat16*>(out), lse, ws,
+      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t qsa_sparse_attn_decode_multi_workspace(const qsa_config* cfg, int64_t B, int32_t n_q, int32_t Hq,
+                                              int32_t Hkv) {
+  if (check_config(cfg) != QSA_OK || B < 0 || n_q < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return 0;
+  return align_up(decode_workspace_bytes(B * n_q, Hq, Hkv, k_blocks(cfg), cfg->r));
+}
+
+qsa_status qsa_sparse_attn_decode_multi(const qsa_config* cfg, const void* q, const void* k_cache,
+                                        const void* v_cache, int64_t L_cap, const int64_t* cache_len,
+                                        const int32_t* idx, const int32_t* count, int64_t B, int32_t n_q,
+                                        int32_t Hq, int32_t Hkv, float scale, void* out, float* lse, void* ws,
+                                        size_t ws_bytes, qsa_stream_t stream) {
+  qsa_status s = check_config(cfg);
+  if (s != QSA_OK) return s;
+  if (B < 0 || n_q < 1 || L_cap < 0 || Hq < 1 || Hkv < 1 || !std::isfinite(scale)) return QSA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return QSA_ERR_UNSUPPORTED;
+  if (B == 0) return QSA_OK;
+  if (!q || !k_cache || !v_cache || !cache_len || !idx || !count || !out || L_cap < 1)
+    return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return QSA_ERR_INVALID_ARG;
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return QSA_ERR_INVALID_ARG;
+  if (ws_bytes < qsa_sparse_attn_decode_multi_workspace(cfg, B, n_q, Hq, Hkv)) return QSA_ERR_WORKSPACE;
+  return from_cuda(launch_sparse_attn_decode(
+      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_cache),
+      static_cast<const __nv_bfloat16*>(v_cache), L_cap, cache_len, idx, count, B, n_q, Hq, Hkv,
       cfg->r, k_blocks(cfg), scale, static_cast<__nv_bfloat16*>(out), lse, ws,
       reinterpret_cast<cudaStream_t>(stream)));
 }

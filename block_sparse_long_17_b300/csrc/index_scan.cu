@@ -133,15 +133,19 @@ cudaError_t launch_index_scan(const __nv_bfloat16* qt, const __nv_bfloat16* kbar
 }
 
 
-// Decode scan: one query row per sequence.  A persistent grid of warps splits
-// the (sequence, 16-block tile) space into equal contiguous ranges, so every
-// warp streams the same number of k-bar rows and none is left for a tail wave.
-// Within a range the 16-block tiles are double-buffered in registers (the next
-// tile's 8 loads per lane are in flight while the current tile's MMAs run).
-// MMA columns 0-3 are the 4 indexer heads, 4-7 are zero.
+// Decode scan: up to 4 query rows per sequence (one new token, or the n_q
+// tokens of a multi-token step), all scored in the same pass over k-bar.  A
+// persistent grid of warps splits the (sequence, 16-block tile) space into
+// equal contiguous ranges, so every warp streams the same number of k-bar rows
+// and none is left for a tail wave.  Within a range the 16-block tiles are
+// double-buffered in registers (the next tile's 8 loads per lane are in flight
+// while the current tile's MMAs run).  MMA n-tile j holds query rows 2j and
+// 2j + 1 (4 heads each; a missing row is zero).  Every row is scored up to the
+// sequence's largest visible block; the selection applies each row's own range.
+template <int NT>
 __global__ void __launch_bounds__(kScanWarps * 32)
 decode_scan_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16* __restrict__ kbar,
-                   int64_t kbar_stride_b, const int64_t* __restrict__ q_pos, int64_t B, int r,
+                   int64_t kbar_stride_b, const int64_t* __restrict__ q_pos, int64_t B, int n_q, int r,
                    int64_t c_cap, int64_t tiles_per_seq, int64_t tiles_per_warp, float* __restrict__ S,
                    int64_t s_stride) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -153,7 +157,7 @@ decode_scan_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16* __
   while (t0 < t1) {
     const int64_t bb = t0 / tiles_per_seq;
     const int64_t seg_end = (bb + 1) * tiles_per_seq < t1 ? (bb + 1) * tiles_per_seq : t1;
-    int64_t c = (q_pos[bb] + 1) / r;
+    int64_t c = (q_pos[bb] + n_q) / r;  // blocks the sequence's last row sees
     if (c > c_cap) {
       if (lane == 0 && t0 == bb * tiles_per_seq) flag_device_error(kDevErrPosition);
       c = c_cap;
@@ -163,17 +167,19 @@ decode_scan_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16* __
     const int64_t b_end = b_lim < c ? b_lim : c;
     t0 = seg_end;
     if (b_begin >= b_end) continue;
-    uint32_t qf[16];
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(qt + (bb * kIdxHeads + (gid & 3)) * kHeadDim + 32 * t);
+    uint32_t qf[NT][16];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int qrow = 2 * j + (gid >> 2);
+      const uint4* src =
+          reinterpret_cast<const uint4*>(qt + ((bb * n_q + qrow) * kIdxHeads + (gid & 3)) * kHeadDim + 32 * t);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const uint4 v = gid < 4 ? src[u] : make_uint4(0, 0, 0, 0);
-        qf[4 * u + 0] = v.x; qf[4 * u + 1] = v.y; qf[4 * u + 2] = v.z; qf[4 * u + 3] = v.w;
+        const uint4 v = qrow < n_q ? src[u] : make_uint4(0, 0, 0, 0);
+        qf[j][4 * u + 0] = v.x; qf[j][4 * u + 1] = v.y; qf[j][4 * u + 2] = v.z; qf[j][4 * u + 3] = v.w;
       }
     }
     const __nv_bfloat16* kb = kbar + bb * kbar_stride_b;
-    float* srow = S + bb * s_stride;
     auto load_tile = [&](int64_t b0, uint32_t (&ka)[16], uint32_t (&kx)[16]) {
       const int64_t ra = b0 + gid < b_end ? b0 + gid : b_end - 1;
       const int64_t rb = b0 + gid + 8 < b_end ? b0 + gid + 8 : b_end - 1;
@@ -191,20 +197,28 @@ decode_scan_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16* __
     for (int64_t b0 = b_begin; b0 < b_end; b0 += 16) {
       const bool more = b0 + 16 < b_end;
       if (more) load_tile(b0 + 16, na, nx);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t a[4] = {ka[2 * ks], kx[2 * ks], ka[2 * ks + 1], kx[2 * ks + 1]};
-        const uint32_t b[2] = {qf[2 * ks], qf[2 * ks + 1]};
-        mma_bf16_16816(acc, a, b);
+      for (int j = 0; j < NT; ++j) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t a[4] = {ka[2 * ks], kx[2 * ks], ka[2 * ks + 1], kx[2 * ks + 1]};
+          const uint32_t bq[2] = {qf[j][2 * ks], qf[j][2 * ks + 1]};
+          mma_bf16_16816(acc, a, bq);
+        }
+        // acc: (block b0+gid, columns 2t, 2t+1), (b0+gid+8, 2t, 2t+1); column
+        // 4 q' + h is head h of query row 2j + q'.
+        float sa = fmaxf(acc[0], 0.f) + fmaxf(acc[1], 0.f);
+        float sb = fmaxf(acc[2], 0.f) + fmaxf(acc[3], 0.f);
+        sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+        sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+        const int qrow = 2 * j + (t >> 1);
+        if ((t & 1) == 0 && qrow < n_q) {
+          float* srow = S + (bb * n_q + qrow) * s_stride;
+          if (b0 + gid < b_end) srow[b0 + gid] = sa;
+          if (b0 + gid + 8 < b_end) srow[b0 + gid + 8] = sb;
+        }
       }
-      // acc: (block b0+gid, heads 2t, 2t+1), (b0+gid+8, heads 2t, 2t+1); heads >= 4 are zero.
-      float sa = fmaxf(acc[0], 0.f) + fmaxf(acc[1], 0.f);
-      float sb = fmaxf(acc[2], 0.f) + fmaxf(acc[3], 0.f);
-      sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-      sb += __shfl_xor_sync(0xffffffffu, sb, 1);
-      if (t == 0 && b0 + gid < b_end) srow[b0 + gid] = sa;
-      if (t == 0 && b0 + gid + 8 < b_end) srow[b0 + gid + 8] = sb;
       if (more) {
 #pragma unroll
         for (int u = 0; u < 16; ++u) { ka[u] = na[u]; kx[u] = nx[u]; }
@@ -213,13 +227,13 @@ decode_scan_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16* __
   }
 }
 
-cudaError_t launch_decode_scan(const __nv_bfloat16* qt, const __nv_bfloat16* kbar, int64_t kbar_stride_b,
-                               const int64_t* q_pos, int64_t B, int r, int64_t c_max, float* S,
-                               int64_t s_stride, cudaStream_t st) {
-  if (B <= 0 || c_max <= 0) return cudaSuccess;
+template <int NT>
+static cudaError_t launch_decode_scan_nt(const __nv_bfloat16* qt, const __nv_bfloat16* kbar, int64_t kbar_stride_b,
+                                         const int64_t* q_pos, int64_t B, int n_q, int r, int64_t c_max, float* S,
+                                         int64_t s_stride, cudaStream_t st) {
   static int blocks_per_sm = 0;
   if (blocks_per_sm == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, decode_scan_kernel,
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, decode_scan_kernel<NT>,
                                                                   kScanWarps * 32, 0);
     if (e != cudaSuccess) return e;
     if (blocks_per_sm < 1) blocks_per_sm = 1;
@@ -235,9 +249,22 @@ cudaError_t launch_decode_scan(const __nv_bfloat16* qt, const __nv_bfloat16* kba
   const int64_t tiles_per_warp = (total + warps - 1) / warps;
   warps = (total + tiles_per_warp - 1) / tiles_per_warp;
   const int64_t grid = (warps + kScanWarps - 1) / kScanWarps;
-  decode_scan_kernel<<<(unsigned)grid, kScanWarps * 32, 0, st>>>(qt, kbar, kbar_stride_b, q_pos, B, r, c_max,
-                                                                 tiles_per_seq, tiles_per_warp, S, s_stride);
+  decode_scan_kernel<NT><<<(unsigned)grid, kScanWarps * 32, 0, st>>>(qt, kbar, kbar_stride_b, q_pos, B, n_q, r, c_max,
+                                                                     tiles_per_seq, tiles_per_warp, S, s_stride);
   return count_launch(cudaGetLastError());
+}
+
+// Scores of the n_q <= kDecodeMaxRows query rows of each sequence in one pass
+// over k-bar; rows bb * n_q + j of S.
+constexpr int kDecodeMaxRows = 4;
+
+cudaError_t launch_decode_scan(const __nv_bfloat16* qt, const __nv_bfloat16* kbar, int64_t kbar_stride_b,
+                               const int64_t* q_pos, int64_t B, int n_q, int r, int64_t c_max, float* S,
+                               int64_t s_stride, cudaStream_t st) {
+  if (B <= 0 || c_max <= 0 || n_q <= 0) return cudaSuccess;
+  if (n_q > kDecodeMaxRows) return cudaErrorInvalidValue;
+  return n_q <= 2 ? launch_decode_scan_nt<1>(qt, kbar, kbar_stride_b, q_pos, B, n_q, r, c_max, S, s_stride, st)
+                  : launch_decode_scan_nt<2>(qt, kbar, kbar_stride_b, q_pos, B, n_q, r, c_max, S, s_stride, st);
 }
 
 }  // namespace qsa

@@ -283,8 +283,10 @@ sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
   }
 }
 
-// Decode: persistent warps over (sequence, kv head, 8-head chunk, split)
-// items; a split is `split_len` consecutive slots.  A warp writes unnormalised O
+// Decode: persistent warps over (query row, kv head, 8-head chunk, split)
+// items; a split is `split_len` consecutive slots.  Sequence bb holds n_q new
+// query rows (one for plain decode), row j at position cache_len[bb] - n_q + j,
+// all reading the sequence's K/V cache.  A warp writes unnormalised O
 // (fp32) with its running max and sum per head, then counts itself in the
 // unit's counter; the warp that completes the count combines the unit's
 // splits (log-sum-exp weights) into the bf16 output and resets the counter.
@@ -345,8 +347,8 @@ __global__ void __launch_bounds__(kAWarps * 32, 1)
 sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                           const __nv_bfloat16* __restrict__ v, int64_t L_cap,
                           const int64_t* __restrict__ cache_len, const int32_t* __restrict__ idx,
-                          const int32_t* __restrict__ count, int64_t B, int Hq, int Hkv, int r, int k_b,
-                          int n_split, int split_len, float scale, float* __restrict__ part_o,
+                          const int32_t* __restrict__ count, int64_t B, int n_q, int Hq, int Hkv, int r,
+                          int k_b, int n_split, int split_len, float scale, float* __restrict__ part_o,
                           float* __restrict__ part_ml, int* __restrict__ unit_done,
                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   extern __shared__ __align__(128) uint8_t attn_smem[];
@@ -355,15 +357,16 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(wbuf));
   const int group = Hq / Hkv;
   const int n_hc = (group + 7) / 8;
-  const int64_t items = B * Hkv * n_hc * n_split;
+  const int64_t items = B * n_q * Hkv * n_hc * n_split;
   const int64_t nwarps = (int64_t)gridDim.x * kAWarps;
   for (int64_t item = (int64_t)blockIdx.x * kAWarps + warp; item < items; item += nwarps) {
     const int split = (int)(item % n_split);
-    const int64_t wi = item / n_split;          // (bb, g, hc)
+    const int64_t wi = item / n_split;          // (row, g, hc)
     const int hc = (int)(wi % n_hc);
     const int g = (int)((wi / n_hc) % Hkv);
-    const int64_t bb = wi / (n_hc * Hkv);
-    const int64_t i = cache_len[bb] - 1;
+    const int64_t row = wi / (n_hc * Hkv);      // bb * n_q + j
+    const int64_t bb = row / n_q;
+    const int64_t i = cache_len[bb] - n_q + row % n_q;
     const int qh0 = g * group + 8 * hc;
     const int n_heads = min(8, group - 8 * hc);
     float* po = part_o + (wi * n_split + split) * (8 * kHeadDim);
@@ -375,7 +378,7 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
       if (lane == 0 && split == 0) flag_device_error(kDevErrPosition);
       empty = true;
     } else {
-      a = make_row(i, r, idx + bb * (int64_t)k_b, count[bb], k_b);
+      a = make_row(i, r, idx + row * (int64_t)k_b, count[row], k_b);
       s_beg = split * split_len;
       s_end = min(a.n_tok, s_beg + split_len);
       empty = s_beg >= s_end;  // an empty split contributes nothing
@@ -386,7 +389,7 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
       const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
       const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
       float o[8][4], m2[2], l[2];
-      attend_slots(q + (bb * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end, scale * kLog2e, ring, o,
+      attend_slots(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end, scale * kLog2e, ring, o,
                    m2, l);
       float* st = reinterpret_cast<float*>(wbuf);
       stage_o(st, o, 1.f, 1.f);
@@ -408,7 +411,7 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
     if (last) {
       __threadfence();
       combine_unit(part_o + wi * n_split * (8 * kHeadDim), part_ml + wi * n_split * 16, n_split, n_heads,
-                   out + (bb * Hq + qh0) * kHeadDim, lse != nullptr ? lse + bb * Hq + qh0 : nullptr);
+                   out + (row * Hq + qh0) * kHeadDim, lse != nullptr ? lse + row * Hq + qh0 : nullptr);
       if (lane == 0) unit_done[wi] = 0;
     }
     __syncwarp();
@@ -469,11 +472,11 @@ cudaError_t launch_sparse_attn_prefill(const __nv_bfloat16* q, const __nv_bfloat
 cudaError_t launch_sparse_attn_decode(const __nv_bfloat16* q, const __nv_bfloat16* k,
                                       const __nv_bfloat16* v, int64_t L_cap,
                                       const int64_t* cache_len, const int32_t* idx,
-                                      const int32_t* count, int64_t B, int Hq, int Hkv, int r,
+                                      const int32_t* count, int64_t B, int n_q, int Hq, int Hkv, int r,
                                       int k_b, float scale, __nv_bfloat16* out, float* lse,
                                       void* ws, cudaStream_t st) {
   const int n_hc = (Hq / Hkv + 7) / 8;
-  const int64_t units = B * Hkv * n_hc;
+  const int64_t units = B * n_q * Hkv * n_hc;
   if (units == 0) return cudaSuccess;
   const int max_split = decode_max_splits(k_b, r);
   float* part_o = reinterpret_cast<float*>(ws);
@@ -501,7 +504,7 @@ cudaError_t launch_sparse_attn_decode(const __nv_bfloat16* q, const __nv_bfloat1
   e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), 1, units * n_split, &grid);
   if (e != cudaSuccess) return e;
   sparse_attn_decode_kernel<<<grid, kAWarps * 32, kASmemBytes, st>>>(
-      q, k, v, L_cap, cache_len, idx, count, B, Hq, Hkv, r, k_b, (int)n_split, split_len, scale, part_o, part_ml,
+      q, k, v, L_cap, cache_len, idx, count, B, n_q, Hq, Hkv, r, k_b, (int)n_split, split_len, scale, part_o, part_ml,
       unit_done, out, lse);
   return count_launch(cudaGetLastError());
 }

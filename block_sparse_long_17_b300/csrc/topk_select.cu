@@ -410,14 +410,13 @@ topk_select_fast_kernel(const float* __restrict__ S, int64_t s_stride, const int
 }
 
 // ---------------------------------------------------------------------------------------------
-// The same selection with each row split over a cluster of kSelCluster CTAs
-// (decode: few rows, long rows).  Every CTA takes a quarter of the row: local
+// The same selection with each row split over a cluster of kSelCluster = 4
+// CTAs (decode: few rows, long rows).  Every CTA takes a quarter of the row: local
 // histograms of the top 11 bits, merged by every CTA through distributed
 // shared memory; ordered copies of the entries at or above the boundary bin,
 // gathered into the first CTA's candidate arrays in rank (= block) order; that
 // CTA refines and emits.
-constexpr int kSelCluster = 4;
-
+template <int kSelCluster>
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
 topk_select_cluster_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t* __restrict__ q_pos,
                            int64_t n_q, int64_t row_lo, int r, int k_b, int64_t c_cap,
@@ -564,8 +563,8 @@ cudaError_t launch_topk_select_cluster(const float* S, int64_t s_stride, const i
                                        int64_t row_lo, int64_t n_rows, int r, int k_b, int64_t c_cap,
                                        int32_t* idx, int32_t* count, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
-  topk_select_cluster_kernel<<<(unsigned)(n_rows * kSelCluster), kSelThreads, 0, st>>>(
-      S, s_stride, q_pos, n_q, row_lo, r, k_b, c_cap, idx, count);
+  topk_select_cluster_kernel<4><<<(unsigned)(n_rows * 4), kSelThreads, 0, st>>>(S, s_stride, q_pos, n_q, row_lo,
+                                                                                r, k_b, c_cap, idx, count);
   return count_launch(cudaGetLastError());
 }
 

@@ -27,6 +27,7 @@ EXPORTED = [
     "qsa_default_config", "qsa_num_selected_blocks", "qsa_compress_keys",
     "qsa_index_topk_workspace", "qsa_index_topk", "qsa_sparse_attn_prefill",
     "qsa_sparse_attn_decode_workspace", "qsa_sparse_attn_decode", "qsa_sparse_attn_decode_noalloc",
+    "qsa_sparse_attn_decode_multi_workspace", "qsa_sparse_attn_decode_multi",
     "qsa_probe_l2_gather", "qsa_status_string",
     "qsa_read_device_error", "qsa_launch_count", "qsa_version",
 ]
@@ -87,6 +88,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qsa_sparse_attn_prefill": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I64, I32, I32, F, P, P, P]),
         "qsa_sparse_attn_decode_workspace": (SZ, [C, I64, I32, I32]),
         "qsa_sparse_attn_decode": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, F, P, P, P, SZ, P]),
+        "qsa_sparse_attn_decode_multi_workspace": (SZ, [C, I64, I32, I32, I32]),
+        "qsa_sparse_attn_decode_multi": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, I32, F, P, P, P, SZ,
+                                                        P]),
         "qsa_sparse_attn_decode_noalloc": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, F, P, P, P]),
         "qsa_probe_l2_gather": (ctypes.c_int, [P, SZ, ctypes.POINTER(ctypes.c_float), P]),
         "qsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -202,6 +206,32 @@ def qsa_sparse_attn_decode(cfg: Config, q: torch.Tensor, k_cache: torch.Tensor,
     _check("qsa_sparse_attn_decode", load_library().qsa_sparse_attn_decode(
         ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), L_cap, _ptr(cache_len), _ptr(idx),
         _ptr(count), B, Hq, Hkv, scale, _ptr(out), _ptr(lse), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def qsa_sparse_attn_decode_multi_workspace(cfg: Config, B: int, n_q: int, Hq: int, Hkv: int) -> int:
+    c = cfg.c_struct()
+    return int(load_library().qsa_sparse_attn_decode_multi_workspace(ctypes.byref(c), B, n_q, Hq, Hkv))
+
+
+def qsa_sparse_attn_decode_multi(cfg: Config, q: torch.Tensor, k_cache: torch.Tensor,
+                                 v_cache: torch.Tensor, cache_len: torch.Tensor, idx: torch.Tensor,
+                                 count: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                                 lse: torch.Tensor | None = None, scale: float | None = None,
+                                 stream=None) -> None:
+    """q [B, n_q, Hq, d]; caches [B, Hkv, L_cap, d]; cache_len [B] int64 (device, includes
+    the n_q new tokens); idx [B, n_q, k_B]; count [B, n_q]; out like q."""
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (out, "out")):
+        _bf16(t, nm)
+    _i64(cache_len, "cache_len")
+    B, n_q, Hq, d = q.shape
+    Hkv, L_cap = k_cache.shape[1], k_cache.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    c = cfg.c_struct()
+    _check("qsa_sparse_attn_decode_multi", load_library().qsa_sparse_attn_decode_multi(
+        ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), L_cap, _ptr(cache_len), _ptr(idx),
+        _ptr(count), B, n_q, Hq, Hkv, scale, _ptr(out), _ptr(lse), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)))
 
 

@@ -65,14 +65,15 @@ class DecodeSpec:
     hq: int = 16
     hkv: int = 2
     extra_cap: int = 4          # spare cache slots past the new token
+    next_n: int = 1             # new tokens per step (the token plus its draft tokens)
 
     @property
     def k_b(self) -> int:
         return -(-self.k_tokens // self.r)
 
     @property
-    def cache_len(self) -> int:  # includes the new token
-        return self.ctx + 1
+    def cache_len(self) -> int:  # includes the new tokens
+        return self.ctx + self.next_n
 
     @property
     def n_blocks(self) -> int:   # compressed blocks the new token can score
@@ -92,6 +93,8 @@ WORKLOADS = {
     # A smaller decode step of the same shape family (a few GB on the device),
     # for profiling captures.
     "decode_64k_x64": DecodeSpec("decode_64k_x64", batch=64, ctx=65536, k_tokens=2048, seed=5),
+    # Multi-token decode as timed in the pages' decode panels: batch 4, next_n = 4, 1M context.
+    "decode_1m_b4_next4": DecodeSpec("decode_1m_b4_next4", batch=4, ctx=1048576 - 4, k_tokens=2048, seed=6, next_n=4),
 }
 
 
@@ -146,20 +149,22 @@ def make_decode(spec: DecodeSpec, device="cpu", *, batch: int | None = None, ctx
     """Draw one decode step: new-token queries, compressed-key cache and KV cache.
 
     The compressed-key cache is drawn directly (already pooled and rotated), as
-    N(0, 1) bf16, for the n_blocks blocks the new token can score.  The KV cache
-    holds cache_len = ctx + 1 valid tokens (the last one is the new token).
+    N(0, 1) bf16, for the n_blocks blocks the last new token can score.  The KV
+    cache holds cache_len = ctx + next_n valid tokens (the last next_n are the
+    new tokens, queried together).
     """
     B = spec.batch if batch is None else batch
     ctx = spec.ctx if ctx is None else ctx
-    cache_len = ctx + 1
+    nn = spec.next_n
+    cache_len = ctx + nn
     n_blocks = cache_len // spec.r
     l_cap = cache_len + spec.extra_cap
     d = spec.d
     gen = torch.Generator(device=device)
     gen.manual_seed(spec.seed)
-    q_idx = _randn_bf16((B, 1, spec.h_idx, d), gen, device)
+    q_idx = _randn_bf16((B, nn, spec.h_idx, d), gen, device)
     kbar = _randn_bf16((B, n_blocks, d), gen, device)
-    q = _randn_bf16((B, 1, spec.hq, d), gen, device)
+    q = _randn_bf16((B, nn, spec.hq, d), gen, device)
     k = torch.empty((B, spec.hkv, l_cap, d), dtype=torch.bfloat16, device=device)
     v = torch.empty((B, spec.hkv, l_cap, d), dtype=torch.bfloat16, device=device)
     for bb in range(B):  # per sequence, to bound the fp32 temporaries

@@ -174,6 +174,31 @@ qsa_status qsa_sparse_attn_decode(const qsa_config* cfg, const void* q, const vo
                                   int32_t Hkv, float scale, void* out, float* lse, void* ws,
                                   size_t ws_bytes, qsa_stream_t stream);
 
+/* Workspace for qsa_sparse_attn_decode_multi with the same (cfg, B, n_q, Hq, Hkv). */
+size_t qsa_sparse_attn_decode_multi_workspace(const qsa_config* cfg, int64_t B, int32_t n_q,
+                                              int32_t Hq, int32_t Hkv);
+
+/*
+ * Multi-token decode: n_q new tokens per sequence in one step ([F6] decode
+ * mode with next_n = 4, i.e. the query token plus three MTP draft tokens).
+ * Row j of sequence bb is token i = cache_len[bb] - n_q + j; each row attends
+ * over its own selection and tail exactly as qsa_sparse_attn_prefill does for
+ * that row, split over the selected tokens and combined with log-sum-exp
+ * weights.  Select the rows with qsa_index_topk(n_q, q_pos = cache_len - n_q):
+ * for n_q <= 4 it scores all rows of a sequence in one pass over kbar.
+ *   q          bf16 [B][n_q][Hq][head_dim]
+ *   k_cache, v_cache  bf16 [B][Hkv][L_cap][head_dim]
+ *   cache_len  device int64 [B]: valid tokens including the n_q new ones (<= L_cap).
+ *   idx, count int32 [B][n_q][k_B], [B][n_q] from qsa_index_topk.
+ *   out        bf16 [B][n_q][Hq][head_dim];  lse fp32 [B][n_q][Hq] or NULL.
+ *   n_q >= 1; with n_q = 1 this is qsa_sparse_attn_decode.
+ */
+qsa_status qsa_sparse_attn_decode_multi(const qsa_config* cfg, const void* q, const void* k_cache,
+                                        const void* v_cache, int64_t L_cap, const int64_t* cache_len,
+                                        const int32_t* idx, const int32_t* count, int64_t B,
+                                        int32_t n_q, int32_t Hq, int32_t Hkv, float scale, void* out,
+                                        float* lse, void* ws, size_t ws_bytes, qsa_stream_t stream);
+
 /*
  * Size of the static scratch array behind qsa_sparse_attn_decode_noalloc.
  * Every device that loads the library holds this much device memory for it

@@ -288,6 +288,71 @@ def test_decode_full_size_sampled_sequences():
         check_decode_seq(cfg, wl, bb, idx, cnt, out, lse)
 
 
+def run_decode_multi(cfg, wl, Hq=16, Hkv=2):
+    """Multi-token decode step: all next_n rows of each sequence selected in one
+    qsa_index_topk call, then qsa_sparse_attn_decode_multi.  Results stay on the device."""
+    B, nn = wl["batch"], wl["q"].shape[1]
+    q_pos = wl["cache_lens"] - nn
+    idx = torch.empty((B, nn, cfg.k_b), dtype=torch.int32, device=DEV)
+    cnt = torch.empty((B, nn), dtype=torch.int32, device=DEV)
+    ws = torch.empty((qsa.qsa_index_topk_workspace(cfg, B, nn, wl["n_blocks"]),), dtype=torch.uint8, device=DEV)
+    qsa.qsa_index_topk(cfg, wl["q_idx"], wl["kbar"], q_pos, wl["n_blocks"], idx, cnt, ws)
+    out = torch.empty_like(wl["q"])
+    lse = torch.empty((B, nn, Hq), dtype=torch.float32, device=DEV)
+    wsa = torch.empty((qsa.qsa_sparse_attn_decode_multi_workspace(cfg, B, nn, Hq, Hkv),), dtype=torch.uint8,
+                      device=DEV)
+    qsa.qsa_sparse_attn_decode_multi(cfg, wl["q"], wl["k"], wl["v"], wl["cache_lens"], idx, cnt, out, wsa, lse)
+    torch.cuda.synchronize()
+    assert qsa.qsa_read_device_error() == 0
+    return idx, cnt, out, lse
+
+
+def check_decode_multi_seq(cfg, wl, bb, idx, cnt, out, lse):
+    """Rows j of sequence bb are tokens L - next_n + j; the oracle scores them
+    against the given compressed-key cache like prefill rows at those positions."""
+    L, nn = int(wl["cache_lens"][bb]), wl["q"].shape[1]
+    res = O.prefill_rows(QC.bf16_to_np32(wl["q_idx"][bb]), None, QC.bf16_to_np32(wl["q"][bb]),
+                         QC.bf16_to_np32(wl["k"][bb]), QC.bf16_to_np32(wl["v"][bb]), range(nn), r=cfg.r,
+                         k_tokens=cfg.k_tokens, q_pos0=L - nn, rope_dims=cfg.rope_dims, rope_base=cfg.rope_base,
+                         kbar=QC.bf16_to_np(wl["kbar"][bb]))
+    return QC.compare_prefill(res, idx[bb].cpu().numpy(), cnt[bb].cpu().numpy(), out[bb].float().cpu().numpy(),
+                              lse[bb].cpu().numpy(), cfg.k_b, cfg.r)
+
+
+@pytest.mark.parametrize("next_n,ctx", [(2, 3001), (3, 5003), (4, 4096), (4, 700)])
+def test_multi_token_decode_matches_oracle(next_n, ctx):
+    """next_n new tokens per sequence (the token and its draft tokens) scored in
+    one pass over the compressed keys; each row keeps its own selection and tail."""
+    spec = DecodeSpec("dm", batch=3, ctx=ctx, k_tokens=512, seed=31, next_n=next_n)
+    wl = make_decode(spec, DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode_multi(cfg, wl)
+    exact = sum(check_decode_multi_seq(cfg, wl, bb, idx, cnt, out, lse)["exact"] for bb in range(3))
+    assert exact >= 3 * next_n - 1
+
+
+def test_multi_token_decode_ragged_cache_lengths():
+    spec = DecodeSpec("dm", batch=3, ctx=3000, k_tokens=256, seed=32, next_n=4)
+    wl = make_decode(spec, DEV)
+    wl["cache_lens"] = torch.tensor([3004, 9, 1207], dtype=torch.int64, device=DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode_multi(cfg, wl)
+    for bb in range(3):
+        check_decode_multi_seq(cfg, wl, bb, idx, cnt, out, lse)
+
+
+@pytest.mark.slow
+def test_multi_token_decode_1m_full_size():
+    """Batch 4, next_n = 4 at a 1M-token cache, as in the bench's multi-token
+    decode line; every row checked."""
+    spec = WORKLOADS["decode_1m_b4_next4"]
+    wl = make_decode(spec, DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode_multi(cfg, wl)
+    exact = sum(check_decode_multi_seq(cfg, wl, bb, idx, cnt, out, lse)["exact"] for bb in range(spec.batch))
+    assert exact >= spec.batch * spec.next_n - 1
+
+
 @pytest.mark.slow
 def test_long_context_chunk_rows_past_bitmap_range():
     """A 128-row chunk at positions 135000.. of a drift workload: every row sees
