@@ -151,6 +151,77 @@ def multi_decode_measure(qsa, spec, steps: int, warmup: int, dev, hbm_gbs: float
                          "frac": achieved / hbm_gbs}}
 
 
+def _median_step_ms(step, steps: int, warmup: int, flush) -> float:
+    import torch
+    for _ in range(max(warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(max(steps, 10)):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def chunked_prefill_measure(qsa, cfg, pspec, wl, pre, chunk: int, steps: int, warmup: int, dev, flush) -> dict:
+    """The pages' chunked-prefill mode: the last `chunk` query rows of the
+    sequence against the whole cached prefix (k-bar already compressed): index +
+    top-k for the chunk's rows, then sparse attention for them."""
+    import torch
+    n = pspec.n
+    lo = n - chunk
+    q_idx = wl["q_idx"][:, lo:].contiguous()
+    q = wl["q"][:, lo:].contiguous()
+    q_pos = torch.full((1,), lo, dtype=torch.int64, device=dev)
+    idx = torch.empty((1, chunk, cfg.k_b), dtype=torch.int32, device=dev)
+    cnt = torch.empty((1, chunk), dtype=torch.int32, device=dev)
+    ws = torch.empty((qsa.qsa_index_topk_workspace(cfg, 1, chunk, pre.n_blocks),), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+
+    def step():
+        qsa.qsa_index_topk(cfg, q_idx, pre.kbar, q_pos, pre.n_blocks, idx, cnt, ws)
+        qsa.qsa_sparse_attn_prefill(cfg, q, wl["k"], wl["v"], q_pos, idx, cnt, out, None)
+
+    ms = _median_step_ms(step, steps, warmup, flush)
+    assert qsa.qsa_read_device_error() == 0
+    return {"chunk_tokens": chunk, "prefix_tokens": lo, "ms_per_chunk": ms, "tokens_per_s": chunk / (ms * 1e-3)}
+
+
+def dense_decode_measure(qsa, dspec, dwl, dq, steps: int, warmup: int, dev, flush, hbm_gbs: float,
+                         qsa_decode_us: float) -> dict:
+    """Dense GQA decode at the decode step's shape, for the pages' form of
+    comparison: the same decode attention kernel with every block of every
+    sequence selected (k_B >= c), i.e. attention over the whole cache.  Its HBM
+    floor (the whole K/V cache read once) is reported beside it."""
+    import torch
+    B, L = dspec.batch, dwl["cache_len"]
+    c = L // dspec.r
+    cfg = qsa.Config(r=dspec.r, k_tokens=c * dspec.r, rope_dims=dspec.rope_dims, rope_base=dspec.rope_base)
+    idx = torch.arange(c, dtype=torch.int32, device=dev).repeat(B, 1).contiguous()
+    cnt = torch.full((B,), c, dtype=torch.int32, device=dev)
+    ws = torch.empty((qsa.qsa_sparse_attn_decode_workspace(cfg, B, dspec.hq, dspec.hkv),), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty((B, dspec.hq, dspec.d), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        qsa.qsa_sparse_attn_decode(cfg, dq, dwl["k"], dwl["v"], dwl["cache_lens"], idx, cnt, out, ws, None)
+
+    ms = _median_step_ms(step, steps, warmup, flush)
+    assert qsa.qsa_read_device_error() == 0
+    kv_bytes = B * dspec.hkv * L * dspec.d * 2 * 2
+    floor_us = kv_bytes / (hbm_gbs * 1e9) * 1e6
+    return {"us_per_step": ms * 1e3, "kv_bytes": kv_bytes, "hbm_floor_us": floor_us,
+            "qsa_decode_us": qsa_decode_us, "speedup_qsa_vs_dense": ms * 1e3 / qsa_decode_us,
+            "speedup_qsa_vs_dense_floor": floor_us / qsa_decode_us,
+            "note": "dense = the decode attention kernel with every block selected; its own numbers, not the pages'"}
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -274,6 +345,8 @@ def main():
     ap.add_argument("--decode-workload", default=DECODE, help="decode workload name, or 'none'")
     ap.add_argument("--multi-decode-workload", default="decode_1m_b4_next4",
                     help="multi-token decode workload timed beside the main step, or 'none'")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the chunked-prefill and dense-decode lines timed after the main step")
     args = ap.parse_args()
 
     import torch
@@ -452,6 +525,13 @@ def main():
         line["decode_us_per_step"] = None
     if decode_multi is not None:
         line["decode_multi"] = decode_multi
+    if not args.no_extras:
+        chunk = min(16384, pspec.n)
+        line["chunked_prefill"] = chunked_prefill_measure(qsa, cfg, pspec, wl, pre, chunk, args.steps, args.warmup,
+                                                          dev, flush)
+        if do_decode:
+            line["dense_decode"] = dense_decode_measure(qsa, dspec, dwl, dq, args.steps, args.warmup, dev, flush,
+                                                        hbm, decode_ms * 1e3)
     if not args.no_e2e and rank == 0 and do_decode:
         line["e2e"] = e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev)
     if not args.no_cpu_baseline and rank == 0 and do_decode:

@@ -293,3 +293,6 @@ const char* qsa_version(void) { return "qsa-b300 0.1 sm_103a"; }
 
 // Measurement helper for the attention roofline.
 #include "probe.cu"
+
+// Diagnostic entry point for the bounded-wait path.
+#include "selftest.cu"

@@ -28,7 +28,7 @@ EXPORTED = [
     "qsa_index_topk_workspace", "qsa_index_topk", "qsa_sparse_attn_prefill",
     "qsa_sparse_attn_decode_workspace", "qsa_sparse_attn_decode", "qsa_sparse_attn_decode_noalloc",
     "qsa_sparse_attn_decode_multi_workspace", "qsa_sparse_attn_decode_multi",
-    "qsa_probe_l2_gather", "qsa_status_string",
+    "qsa_probe_l2_gather", "qsa_selftest_wait_timeout", "qsa_status_string",
     "qsa_read_device_error", "qsa_launch_count", "qsa_version",
 ]
 
@@ -95,6 +95,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qsa_probe_l2_gather": (ctypes.c_int, [P, SZ, ctypes.POINTER(ctypes.c_float), P]),
         "qsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "qsa_read_device_error": (ctypes.c_int, [P]),
+        "qsa_selftest_wait_timeout": (ctypes.c_int, [I64, P]),
         "qsa_launch_count": (ctypes.c_uint64, []),
         "qsa_version": (ctypes.c_char_p, []),
     }
@@ -269,6 +270,12 @@ def qsa_probe_l2_gather(buf: torch.Tensor, stream=None) -> float:
 
 def qsa_read_device_error(stream=None) -> int:
     return int(load_library().qsa_read_device_error(_stream(stream)))
+
+
+def qsa_selftest_wait_timeout(limit_cycles: int, stream=None) -> None:
+    """Diagnostic: a bounded device wait on a barrier nothing arrives on; the
+    timeout then shows in qsa_read_device_error() as QSA_ERR_TIMEOUT."""
+    _check("qsa_selftest_wait_timeout", load_library().qsa_selftest_wait_timeout(int(limit_cycles), _stream(stream)))
 
 
 def qsa_launch_count() -> int:

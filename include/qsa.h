@@ -249,6 +249,18 @@ qsa_status qsa_probe_l2_gather(void* buf, size_t bytes, float* gbs, qsa_stream_t
 const char* qsa_status_string(qsa_status s);
 
 /*
+ * Diagnostic (not part of the method): launches one CTA whose thread waits,
+ * with the library's bounded mbarrier wait, on a barrier that nothing arrives
+ * on.  The wait gives up after limit_cycles SM cycles (1000 .. 4e9), records a
+ * timeout in the device error word exactly as a stalled qsa_index_topk pipeline
+ * would, and the kernel returns normally; qsa_read_device_error then reports
+ * QSA_ERR_TIMEOUT.  Lets a host exercise its timeout handling with no device
+ * fault.  Returns QSA_ERR_INVALID_ARG for a limit outside the range, else the
+ * launch status.
+ */
+qsa_status qsa_selftest_wait_timeout(int64_t limit_cycles, qsa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device error word
  * on the current device (set by a bounded wait that gave up).  Returns QSA_OK,
  * QSA_ERR_TIMEOUT or QSA_ERR_CUDA.

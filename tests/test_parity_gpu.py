@@ -219,6 +219,22 @@ def test_rmsnorm_variant_end_to_end():
     QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, 4)
 
 
+def test_bounded_wait_timeout_reports_and_context_survives():
+    """A device wait that nothing satisfies gives up after its limit (about 1 ms
+    here) and reports QSA_ERR_TIMEOUT through the device error word; the
+    context stays usable and the next prefill still matches the oracle."""
+    assert qsa.qsa_read_device_error() == 0
+    qsa.qsa_selftest_wait_timeout(2_000_000)
+    assert qsa.qsa_read_device_error() == 5  # QSA_ERR_TIMEOUT
+    assert qsa.qsa_read_device_error() == 0  # read and cleared
+    spec, wl = small_case(512, 128, seed=41)
+    cfg = cfg_for(spec)
+    gpu = run_prefill(cfg, wl)
+    res = QC.oracle_rows(wl, [0, 200, 511], cfg=cfg)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, cfg.r)
+    assert st["exact"] >= 2
+
+
 def test_invalid_selection_reports_instead_of_faulting():
     spec, wl = small_case(64, 16, seed=14)
     cfg = cfg_for(spec)
