@@ -49,6 +49,15 @@ def job_tokens_per_s(world: int, tokens_per_rank: int, prefill_ms: float) -> flo
     return world * tokens_per_rank / (prefill_ms * 1e-3)
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# kernel named, at the prefill workload named, from one ncu capture of it:
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum --clock-control none
+#       -k "regex:sparse_attn_prefill" -c 1 python bench.py --decode-workload none
+#       --multi-decode-workload none --no-extras --steps 1 --warmup 3 --no-cpu-baseline --no-e2e
+# A kernel or workload not listed (or a kernel changed since the capture) reports null.
+MEASURED_TRAFFIC = {("attn_prefill", "drift_prefill_128k"): 2298577152 + 544586496}
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -502,7 +511,7 @@ def main():
     dominant = max(["compress", "index_prefill", "attn_prefill"], key=lambda nm: mean[nm])
     roof = dict(roofs[dominant])
     roof["kernel"] = dominant
-    roof["traffic"] = None
+    roof["traffic"] = MEASURED_TRAFFIC.get((dominant, pspec.name))
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
