@@ -4,7 +4,9 @@
 // V row at data-dependent positions; with one kv head's K/V resident in L2 its
 // speed is set by how fast the SMs can gather random 256-byte rows from L2.
 // This kernel measures exactly that on a caller buffer: every half-warp reads
-// one pseudo-randomly chosen 256-byte row (16 lanes x 16 bytes) per step.
+// pseudo-randomly chosen 256-byte rows (16 lanes x 16 bytes), four independent
+// rows per step so that the rate is not limited by one load's latency (more in
+// flight, or 1 KiB segments instead of rows, measured no faster).
 #include "common.cuh"
 
 namespace qsa {
@@ -14,14 +16,18 @@ probe_gather_rows_kernel(const uint4* __restrict__ p, uint64_t nrows, int iters,
   uint32_t acc = 0;
   const int lane = threadIdx.x & 31;
   uint32_t seed = (uint32_t)((blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) / 16) * 2654435761u + 12345u;
-  for (int it = 0; it < iters; ++it) {
-    seed = seed * 1664525u + 1013904223u;
-    const uint64_t row = (seed >> 4) % nrows;
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p + row * 16 + (lane & 15)));
-    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  for (int it = 0; it < iters; it += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      seed = seed * 1664525u + 1013904223u;
+      const uint64_t row = (seed >> 4) % nrows;
+      asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
+                   : "l"(p + row * 16 + (lane & 15)));
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
   }
   if (acc == 0x9e3779b9u) sink[0] = acc;  // keeps the loads alive
 }
