@@ -205,7 +205,7 @@ cudaError_t launch_topk_select(const float* S, int64_t s_stride, const int64_t* 
 
 
 // ---------------------------------------------------------------------------------------------
-// Two-pass variant for long rows: one pass for the histogram of the top 11
+// Two-pass selection for long rows: one pass for the histogram of the top 11
 // bits, one ordered pass that copies every entry at or above the boundary bin
 // into shared memory (at most kSelCand entries, in block order); the remaining
 // refinement and the emission run on that copy.  Rows whose boundary bin is
@@ -303,110 +303,6 @@ __device__ void select_from_candidates(SelectFastSmem& sm, int ncand, uint32_t l
     }
     wr += wtot;
   }
-}
-
-__device__ void cta_select_row_fast(const float* __restrict__ s, int64_t c, int k_b, int32_t* __restrict__ out,
-                                    SelectFastSmem& sm) {
-  // Pass 1: bins of the top 11 bits of the pattern.
-  for (int j = threadIdx.x; j < kSelBins; j += kSelThreads) sm.base.hist[j] = 0;
-  __syncthreads();
-  const int64_t c4 = c & ~int64_t(3);
-#pragma unroll 4
-  for (int64_t e = 4 * (int64_t)threadIdx.x; e < c4; e += 4 * kSelThreads) {
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(s + e));
-    atomicAdd(&sm.base.hist[score_key(x.x) >> 20], 1);
-    atomicAdd(&sm.base.hist[score_key(x.y) >> 20], 1);
-    atomicAdd(&sm.base.hist[score_key(x.z) >> 20], 1);
-    atomicAdd(&sm.base.hist[score_key(x.w) >> 20], 1);
-  }
-  for (int64_t e = c4 + threadIdx.x; e < c; e += kSelThreads) atomicAdd(&sm.base.hist[score_key(__ldcg(s + e)) >> 20], 1);
-  __syncthreads();
-  const int base_bin = (kSelThreads - 1 - threadIdx.x) * kSelBinsPerThread;
-  int loc[kSelBinsPerThread];
-  int sum = 0;
-#pragma unroll
-  for (int q = 0; q < kSelBinsPerThread; ++q) {
-    loc[q] = sm.base.hist[base_bin + kSelBinsPerThread - 1 - q];
-    sum += loc[q];
-  }
-  const int above0 = block_exclusive_scan(sum, sm.base.warp_sums, &sm.base.total);
-  if (above0 < k_b && above0 + sum >= k_b) {
-    int above = above0;
-#pragma unroll
-    for (int q = 0; q < kSelBinsPerThread; ++q) {
-      if (above + loc[q] >= k_b) {
-        const int bin = base_bin + kSelBinsPerThread - 1 - q;
-        sm.base.lo = (uint32_t)bin << 20;
-        sm.base.hi = ((uint32_t)bin << 20) | 0xfffffu;
-        sm.base.need = k_b - above;
-        sm.base.done = above + loc[q];  // entries at or above the bin
-        break;
-      }
-      above += loc[q];
-    }
-  }
-  __syncthreads();
-  uint32_t lo = sm.base.lo, hi = sm.base.hi;
-  int need = sm.base.need;
-  const int ncand = sm.base.done;
-  __syncthreads();
-  if (ncand > kSelCand) {  // boundary bin too full for the copy: general path
-    cta_select_row(s, c, k_b, out, sm.base);
-    return;
-  }
-  // Pass 2: ordered copy of the entries with pattern >= lo.
-  int written = 0;
-  for (int64_t e0 = 0; e0 < c; e0 += 4 * kSelThreads) {
-    const int64_t e = e0 + 4 * threadIdx.x;
-    float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (e + 3 < c) x4 = __ldcg(reinterpret_cast<const float4*>(s + e));
-    const float xs[4] = {x4.x, x4.y, x4.z, x4.w};
-    uint32_t uk[4], take = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uk[q] = 0;
-      if (e + q < c) {
-        uk[q] = score_key(e + 3 < c ? xs[q] : __ldcg(s + e + q));
-        if (uk[q] >= lo) take |= 1u << q;
-      }
-    }
-    const int before = written + block_exclusive_scan(__popc(take), sm.base.warp_sums, &sm.base.total);
-    const int tot = sm.base.total;
-#pragma unroll
-    for (int q = 0, k = 0; q < 4; ++q) {
-      if (take & (1u << q)) {
-        if (before + k < kSelCand) {
-          sm.cu[before + k] = uk[q];
-          sm.cb[before + k] = (int32_t)(e + q);
-        }
-        ++k;
-      }
-    }
-    written += tot;
-  }
-  __syncthreads();
-  select_from_candidates(sm, ncand, lo, hi, need, k_b, out);
-}
-
-// One CTA per row; rows with c <= k_b keep every block.
-__global__ void __launch_bounds__(kSelThreads)
-topk_select_fast_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t* __restrict__ q_pos,
-                        int64_t n_q, int64_t row_lo, int r, int k_b, int64_t c_cap,
-                        int32_t* __restrict__ idx, int32_t* __restrict__ count) {
-  __shared__ SelectFastSmem sm;
-  const int64_t row = row_lo + blockIdx.x;
-  const int64_t bb = row / n_q;
-  const int64_t pos = q_pos[bb] + row % n_q;
-  int64_t c = (pos + 1) / r;
-  if (c > c_cap) c = c_cap;
-  int32_t* out = idx + row * (int64_t)k_b;
-  if (c <= k_b) {
-    for (int j = threadIdx.x; j < k_b; j += kSelThreads) out[j] = j < c ? j : -1;
-    if (threadIdx.x == 0) count[row] = (int32_t)c;
-    return;
-  }
-  cta_select_row_fast(S + (int64_t)blockIdx.x * s_stride, c, k_b, out, sm);
-  if (threadIdx.x == 0) count[row] = k_b;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -568,13 +464,5 @@ cudaError_t launch_topk_select_cluster(const float* S, int64_t s_stride, const i
   return count_launch(cudaGetLastError());
 }
 
-cudaError_t launch_topk_select_fast(const float* S, int64_t s_stride, const int64_t* q_pos, int64_t n_q,
-                                    int64_t row_lo, int64_t n_rows, int r, int k_b, int64_t c_cap, int32_t* idx,
-                                    int32_t* count, cudaStream_t st) {
-  if (n_rows <= 0) return cudaSuccess;
-  topk_select_fast_kernel<<<(unsigned)n_rows, kSelThreads, 0, st>>>(S, s_stride, q_pos, n_q, row_lo, r, k_b, c_cap,
-                                                                    idx, count);
-  return count_launch(cudaGetLastError());
-}
 
 }  // namespace qsa
