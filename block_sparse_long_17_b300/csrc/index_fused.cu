@@ -707,7 +707,7 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 // exact top-k_B of the entries their tile collected (finalize_row), or are
 // queued for the exact fallback kernel when their buffer fell outside
 // [k_B, kFCap] entries or a segment overflowed.
-__global__ void __launch_bounds__(32 * kFinKWarps, 3)
+__global__ void __launch_bounds__(32 * kFinKWarps, 4)
 index_finalize_kernel(const uint2* __restrict__ buf, const int* __restrict__ cnt, const int64_t* __restrict__ q_pos,
                       int64_t n_q, int64_t tiles_per_seq, int64_t t_begin, int64_t t_count, int rshift, int k_b,
                       int64_t c_cap, int32_t* __restrict__ idx, int32_t* __restrict__ count,
