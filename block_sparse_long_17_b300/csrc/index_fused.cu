@@ -62,15 +62,15 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;                 // 512
 constexpr int kPBins = 512;              // pilot bins (1/16 octave), packed 2 per word
 constexpr int kPShift = 19;              // bits below the bin index
 constexpr int kPBase = 1920;             // (bits of 2^-7) >> 19: bins of 2 x score start at 2^-7
-constexpr int kFinRegs = 48;             // entries per lane in finalize
-constexpr int kFCap = 32 * kFinRegs;     // 1536: most entries a token may collect
+constexpr int kFinRegs = 40;             // entries per lane in finalize
+constexpr int kFCap = 32 * kFinRegs;     // 1280 (2.5 k_B at k_B = 512): most entries a token may collect
 constexpr int kSeg = kFCap;              // entries per (token, TMEM lane quarter) segment: a
                                          // quarter may hold all of a row's entries
 constexpr int kFMaxKb = 512;             // largest k_B the fused path handles
 constexpr int kFMaxCtas = 160;           // >= SM count; sizes the buffers
 constexpr int kFMinRows = 64;            // fewer query rows per sequence: scan path
 constexpr int kFbCtas = 148;             // fallback kernel CTAs (one row each at a time)
-constexpr int kTilesPerLaunch = 1024;    // tiles per fused launch (bounds the row buffers: 3 GiB)
+constexpr int kTilesPerLaunch = 1024;    // tiles per fused launch (bounds the row buffers: 1.9 GiB)
 constexpr int kFinKWarps = 4;            // warps per CTA of the finalize kernel
 constexpr uint32_t kABytes = kMB * 128 * 2;     // 32 KB
 constexpr uint32_t kBBytes = kNRows * 128 * 2;  // 48 KB
@@ -233,18 +233,20 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
   FPROF_T0(f0);
   uint32_t ru[kFinRegs];
 #pragma unroll
-  for (int j0 = 0; j0 < kFinRegs; j0 += 16) {  // 16 loads in flight per lane
+  for (int j0 = 0; j0 < kFinRegs; j0 += 16) {  // up to 16 loads in flight per lane
     uint2 xs[16];
 #pragma unroll
     for (int jj = 0; jj < 16; ++jj) {
       const int e = lane + 32 * (j0 + jj);
-      xs[jj] = e < n ? __ldcs(entry_ptr(seg, e, p1, p2, p3)) : make_uint2(0u, 0u);
+      xs[jj] = (j0 + jj < kFinRegs && e < n) ? __ldcs(entry_ptr(seg, e, p1, p2, p3)) : make_uint2(0u, 0u);
     }
 #pragma unroll
     for (int jj = 0; jj < 16; ++jj) {
-      const int e = lane + 32 * (j0 + jj);
-      ru[j0 + jj] = xs[jj].x;
-      if (e < n) ids[e] = (int32_t)xs[jj].y;
+      if (j0 + jj < kFinRegs) {  // resolved at compile time
+        const int e = lane + 32 * (j0 + jj);
+        ru[j0 + jj] = xs[jj].x;
+        if (e < n) ids[e] = (int32_t)xs[jj].y;
+      }
     }
   }
   // Start from the buffer's own pattern range, so the first round's bins are
