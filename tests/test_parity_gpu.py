@@ -211,6 +211,41 @@ def test_chunked_prefill_rows_at_offset():
     assert st["exact"] >= 0.98 * (hi - lo)
 
 
+def test_batched_prefill_sequences_at_different_offsets():
+    """Three sequences in one call, each a 500-row chunk at its own position
+    (0, 1100, 2100) against its own prefix: every (sequence, row) is checked
+    against the oracle run on that sequence alone."""
+    spec = PrefillSpec("b3", n=2600, k_tokens=512, seed=51, batch=3)
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    n_q, offs = 500, [0, 1100, 2100]
+    q_idx = torch.stack([wl["q_idx"][b, o:o + n_q] for b, o in enumerate(offs)]).contiguous()
+    q = torch.stack([wl["q"][b, o:o + n_q] for b, o in enumerate(offs)]).contiguous()
+    nb = spec.n // cfg.r
+    kbar = torch.empty((3, nb, 128), dtype=torch.bfloat16, device=DEV)
+    qsa.qsa_compress_keys(cfg, wl["k_idx"], 0, nb, kbar)
+    q_pos = torch.tensor(offs, dtype=torch.int64, device=DEV)
+    idx = torch.empty((3, n_q, cfg.k_b), dtype=torch.int32, device=DEV)
+    cnt = torch.empty((3, n_q), dtype=torch.int32, device=DEV)
+    ws = torch.empty((qsa.qsa_index_topk_workspace(cfg, 3, n_q, nb),), dtype=torch.uint8, device=DEV)
+    qsa.qsa_index_topk(cfg, q_idx, kbar, q_pos, nb, idx, cnt, ws)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=DEV)
+    qsa.qsa_sparse_attn_prefill(cfg, q, wl["k"], wl["v"], q_pos, idx, cnt, out, lse)
+    torch.cuda.synchronize()
+    assert qsa.qsa_read_device_error() == 0
+    rows = [0, 1, 250, 498, 499]
+    exact = 0
+    for b, o in enumerate(offs):
+        res = O.prefill_rows(QC.bf16_to_np32(q_idx[b]), QC.bf16_to_np(wl["k_idx"][b]), QC.bf16_to_np32(q[b]),
+                             QC.bf16_to_np32(wl["k"][b]), QC.bf16_to_np32(wl["v"][b]), rows, r=cfg.r,
+                             k_tokens=cfg.k_tokens, q_pos0=o, rope_dims=cfg.rope_dims, rope_base=cfg.rope_base)
+        st = QC.compare_prefill(res, idx[b].cpu().numpy(), cnt[b].cpu().numpy(), out[b].float().cpu().numpy(),
+                                lse[b].cpu().numpy(), cfg.k_b, cfg.r)
+        exact += st["exact"]
+    assert exact >= 3 * len(rows) - 1
+
+
 def test_rmsnorm_variant_end_to_end():
     spec, wl = small_case(700, 128, seed=13)
     cfg = cfg_for(spec, rmsnorm=True)
