@@ -654,11 +654,7 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             }
           }
         } else {
-          bool pass = false;
-#pragma unroll
-          for (int k2 = 0; k2 < 16; ++k2) pass |= u16[k2] >= tau16[k2];
-          if (__any_sync(0xffffffffu, pass)) {  // a chunk whose 512 pairs all fall below tau is skipped
-            if (ew == 0 && lane == 0) FPROF_CNT(2, 1);
+          {  // nearly every chunk has some pair above tau, so no pre-check
             const unsigned lt_mask = (1u << lane) - 1u;
             if (chunk_all_visible) {
 #pragma unroll
