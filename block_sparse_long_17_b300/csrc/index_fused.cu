@@ -661,16 +661,18 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
               for (int k2 = 0; k2 < 16; ++k2) {
                 const bool mine = u16[k2] >= tau16[k2];
                 const unsigned tmk = __ballot_sync(0xffffffffu, mine);
-                const int pos = cnt16[k2] + __popc(tmk & lt_mask);
-                if (mine && pos < kSeg) seg0[k2 * 4 * kSeg + pos] = make_uint2(u16[k2], (uint32_t)bi);
+                // An overflowing segment writes its last slot; its count keeps
+                // growing, and the finalize sends such a row to the fallback.
+                const int pos = min(cnt16[k2] + __popc(tmk & lt_mask), kSeg - 1);
+                if (mine) seg0[k2 * 4 * kSeg + pos] = make_uint2(u16[k2], (uint32_t)bi);
                 cnt16[k2] += __popc(tmk);
               }
             } else {
 #pragma unroll
               for (int k2 = 0; k2 < 16; ++k2) {
                 const unsigned tmk = __ballot_sync(0xffffffffu, u16[k2] >= tau16[k2]) & vis_mask(k2);
-                const int pos = cnt16[k2] + __popc(tmk & lt_mask);
-                if (((tmk >> lane) & 1u) && pos < kSeg) seg0[k2 * 4 * kSeg + pos] = make_uint2(u16[k2], (uint32_t)bi);
+                const int pos = min(cnt16[k2] + __popc(tmk & lt_mask), kSeg - 1);
+                if ((tmk >> lane) & 1u) seg0[k2 * 4 * kSeg + pos] = make_uint2(u16[k2], (uint32_t)bi);
                 cnt16[k2] += __popc(tmk);
               }
             }
