@@ -6,12 +6,12 @@
 // indexer heads, top k_B = ceil(K / r) blocks per query; paperglide reader,
 // "Qwen Sparse Attention" step 3 (block-causal mask) and step 4 (top-K_B).
 //
-// Layout of the work.  A persistent CTA takes tiles of 64 consecutive query
+// Layout of the work.  A persistent CTA takes tiles of 48 consecutive query
 // tokens of one sequence.  A chunk is 128 compressed blocks: 8 tcgen05 MMAs
 // (16 head dims each) compute D[row][token * 4 + head] = <kbar_block(row),
-// qt_token^head>: M = 128 rows (A = the kbar chunk, streamed through a 2-stage
-// TMA ring), N = 256 (B = the tile's 64 x 4 rotated query rows, loaded once per
-// tile), fp32 accumulators in TMEM (two buffers of 256 columns).  The tile's
+// qt_token^head>: M = 128 rows (A = the kbar chunk, streamed through a 3-stage
+// TMA ring), N = 192 (B = the tile's 48 x 4 rotated query rows, loaded once per
+// tile), fp32 accumulators in TMEM (two buffers, 256 columns apart).  The tile's
 // visible blocks are split into 4 consecutive regions of R = 32 x nchunks
 // blocks; rows 32 q .. 32 q + 31 of chunk x hold blocks q R + 32 x .. + 31, so
 // TMEM lane quarter q walks region q in order.  A TMEM lane holds the four
@@ -37,7 +37,7 @@
 //      id.  Rows whose buffer fell outside that range are queued for the exact
 //      fallback kernel (score the whole row, radix-select it), so the result is
 //      always exact.
-// Sixteen score warps (four per TMEM lane quarter, 16 tokens each) read the
+// Twelve score warps (three per TMEM lane quarter, 16 tokens each) read the
 // accumulators; the host launches the kernel over ranges of at most
 // kTilesPerLaunch tiles so that the entry buffers stay bounded.
 //
@@ -820,7 +820,7 @@ struct FusedLayout {
 };
 
 // Workspace of the fused path (after the rotated queries): the entry buffers of
-// one launch's tiles (64 tokens x 4 segments x kSeg entries per tile) and their
+// one launch's tiles (48 tokens x 4 segments x kSeg entries per tile) and their
 // counts, the fallback row list and counter, and the fallback kernel's score rows.
 inline FusedLayout fused_layout(int64_t B, int64_t n_q, int64_t n_blocks_max) {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
