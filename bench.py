@@ -231,6 +231,32 @@ def dense_decode_measure(qsa, dspec, dwl, dq, steps: int, warmup: int, dev, flus
             "note": "dense = the decode attention kernel with every block selected; its own numbers, not the pages'"}
 
 
+def dense_prefill_measure(wl, qsa_prefill_ms: float, steps: int, warmup: int, flush) -> dict:
+    """Dense causal GQA over the same prefill (all 131072 rows, every earlier
+    token), for the pages' form of comparison.  This arm is a library kernel
+    (PyTorch scaled_dot_product_attention restricted to its cuDNN / flash
+    backends, never the materialising one), not part of this library."""
+    import torch
+    try:
+        from torch.nn.attention import SDPBackend, sdpa_kernel
+        q = wl["q"].transpose(1, 2).contiguous()  # [B, Hq, n, d]
+        k, v = wl["k"][:, :, :q.shape[2]], wl["v"][:, :, :q.shape[2]]
+
+        def step():
+            with sdpa_kernel([SDPBackend.CUDNN_ATTENTION, SDPBackend.FLASH_ATTENTION]):
+                torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True, enable_gqa=True)
+
+        ms = _median_step_ms(step, min(steps, 5), warmup, flush)
+    except Exception as ex:  # no fused dense backend on this build: report it instead
+        return {"unavailable": str(ex).split("\n")[0][:160]}
+    n, hq, d = q.shape[2], q.shape[1], q.shape[3]
+    flops = 4 * hq * d * n * (n + 1) / 2
+    return {"ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "qsa_prefill_ms": qsa_prefill_ms,
+            "speedup_qsa_vs_dense": ms / qsa_prefill_ms,
+            "note": "dense = library SDPA (cuDNN or flash backend), causal, GQA; QSA = compress + index + "
+                    "sparse attention of this library"}
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -541,6 +567,7 @@ def main():
         if do_decode:
             line["dense_decode"] = dense_decode_measure(qsa, dspec, dwl, dq, args.steps, args.warmup, dev, flush,
                                                         hbm, decode_ms * 1e3)
+        line["dense_prefill"] = dense_prefill_measure(wl, prefill_ms, args.steps, args.warmup, flush)
     if not args.no_e2e and rank == 0 and do_decode:
         line["e2e"] = e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev)
     if not args.no_cpu_baseline and rank == 0 and do_decode:
@@ -573,7 +600,11 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev, chu
     h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + dq_h.numel() * 2 + dqi_h.numel() * 2
     d2h = out_h.numel() * 2 + dout_h.numel() * 2
     n, r, hkv = wl["q"].shape[1], cfg.r, wl["k"].shape[1]
-    chunks = [(lo, min(n, lo + chunk)) for lo in range(0, n, chunk)]
+    # Chunk boundaries offset by half a chunk: the first chunk (whose copy-in
+    # the kernels wait for) is half-size, and so is the last one (whose
+    # copy-out follows them) when n is a multiple of the chunk.
+    bounds = [0] + list(range(min(n, chunk // 2), n, chunk)) + [n]
+    chunks = [(a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
     qpos = [torch.full((1,), lo, dtype=torch.int64, device=dev) for lo, _ in chunks]
     ws_c = torch.empty((qsa.qsa_index_topk_workspace(cfg, 1, min(chunk, n), pre.n_blocks),), dtype=torch.uint8,
                        device=dev)
