@@ -154,10 +154,16 @@ def multi_decode_measure(qsa, spec, steps: int, warmup: int, dev, hbm_gbs: float
     us = statistics.median(ts) * 1e3
     wk = decode_multi_work(B, wl["cache_len"], nn, spec.r, spec.k_b, spec.hq, spec.hkv)
     achieved = wk["bytes"] / (us * 1e-6) / 1e9
+    # Any dense decode of these rows reads the whole K/V cache at least once:
+    # its HBM time is a lower bound on every dense kernel at this shape.
+    kv_bytes = B * spec.hkv * wl["cache_len"] * spec.d * 2 * 2
+    floor_us = kv_bytes / (hbm_gbs * 1e9) * 1e6
     return {"workload": spec.name, "batch": B, "next_n": nn, "ctx_tokens": wl["cache_len"],
             "us_per_step": us, "bytes_per_step": wk["bytes"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                         "frac": achieved / hbm_gbs}}
+                         "frac": achieved / hbm_gbs},
+            "dense_floor": {"kv_bytes": kv_bytes, "hbm_floor_us": floor_us, "speedup_qsa_vs_dense_floor": floor_us / us,
+                            "note": "dense decode of the same rows cannot read less than the whole K/V cache once"}}
 
 
 def _median_step_ms(step, steps: int, warmup: int, flush) -> float:

@@ -15,15 +15,15 @@
 // visible blocks are split into 4 consecutive regions of R = 32 x nchunks
 // blocks; rows 32 q .. 32 q + 31 of chunk x hold blocks q R + 32 x .. + 31, so
 // TMEM lane quarter q walks region q in order.  A TMEM lane holds the four
-// heads of each token in adjacent columns: a thread finishes a score with 7
-// adds (x + |x| is 2 ReLU(x)).
+// heads of each token in adjacent columns: a thread finishes two scores with
+// 8 adds x + |x| (= 2 ReLU(x)) and 3 packed two-lane fp32 adds.
 //
 // Exact selection in one pass over the blocks.
 //   1. Pilot: a strided sample of the tile's blocks (every 16th block, in one
 //      or more phases) is scored first and binned per token into 512 bins of
 //      1/16 octave of the fp32 score (16-bit counters, two per word).  From it
-//      each token takes a threshold tau above which about 1.5 k_B of its scores
-//      are expected.
+//      each token takes a threshold tau above which about 1.6 k_B of its scores
+//      are expected (interpolated inside the bin where the count is reached).
 //   2. Collect: every chunk is scored; each (token, block) with score >= tau is
 //      appended (bit pattern u of 2 x score, block id) to the token's buffer in
 //      global memory: one segment per TMEM lane quarter, so that no two warps
@@ -118,6 +118,8 @@ struct TileMeta {
 
 constexpr int kPilotStride = 16;   // the pilot samples every 16th block (per phase)
 constexpr int kPilotMin = 3072;    // at least this many pilot samples per row when possible
+constexpr int kPilotNum = 8;       // tau aims at kPilotNum / kPilotDen x k_B entries per row:
+constexpr int kPilotDen = 5;       // near the middle, in ratio, of the accepted [k_B, 2.5 k_B]
 
 __device__ __forceinline__ TileMeta tile_meta(int64_t t, int64_t tiles_per_seq, int64_t n_q,
                                               const int64_t* q_pos, int rshift, int k_b, int64_t c_cap) {
@@ -343,11 +345,15 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
 }
 
 // ---------------------------------------------------------------------------------------------
-// Threshold of one token from its pilot histogram (one warp): the lowest bin
-// such that the bins from it upward hold at least ceil(1.5 k_B P / c) of the P
-// samples, as the bit pattern of the bin's lower edge (0 when the bottom bin is
-// reached or the row has no samples, which collects every visible block).  The
-// histogram is cleared for the next tile.  Lane L owns bins 16 (31 - L) .. + 15.
+// Threshold of one token from its pilot histogram (one warp).  want =
+// ceil(kPilotNum k_B P / (kPilotDen c)) of the P samples should lie at or above
+// tau: the bin where the count from the top reaches want is found, and tau is
+// placed inside it by linear interpolation, as if its samples were spread
+// evenly over its value range (the bins are 1/16 octave wide, and in the far
+// tail of a row's scores one bin can hold as many samples as all the bins above
+// it).  tau is 0 when the bottom bin is reached or the row has no samples,
+// which collects every visible block.  The histogram is cleared for the next
+// tile.  Lane L owns bins 16 (31 - L) .. + 15.
 __device__ __forceinline__ uint32_t pilot_tau(uint32_t* __restrict__ hist, int64_t c, int k_b) {
   const int lane = threadIdx.x & 31;
   uint4* const w4 = reinterpret_cast<uint4*>(hist + 8 * (31 - lane));
@@ -369,20 +375,32 @@ __device__ __forceinline__ uint32_t pilot_tau(uint32_t* __restrict__ hist, int64
     if (lane >= o) incl += y;
   }
   const int64_t P = __shfl_sync(0xffffffffu, incl, 31);
-  int64_t want = (3 * (int64_t)k_b * P + 2 * c - 1) / (2 * c);  // ceil(1.5 k_B P / c)
+  int64_t want = (kPilotNum * (int64_t)k_b * P + kPilotDen * c - 1) / (kPilotDen * c);
   if (want < 1) want = 1;
   const int above0 = incl - sum;
   const bool cross = above0 < want && incl >= want;
   uint32_t tau = 0;
   if (cross) {
-    int above = above0;
+    // The first of the lane's bins (from the top) where the count reaches want:
+    // its index, the count above it and its own count (no early exit, so that
+    // loc[] stays in registers).
+    int above = above0, bin = -1, b_above = 0, b_cnt = 1;
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
+      if (bin < 0 && above + loc[q] >= want) {
+        bin = 16 * (31 - lane) + 15 - q;
+        b_above = above;
+        b_cnt = loc[q];
+      }
       above += loc[q];
-      if (above >= want) {
-        const int bin = 16 * (31 - lane) + 15 - q;
-        tau = bin == 0 ? 0u : (uint32_t)(kPBase + bin) << kPShift;
-        break;
+    }
+    if (bin > 0) {
+      tau = (uint32_t)(kPBase + bin) << kPShift;  // lower edge
+      if (bin < kPBins - 1) {  // the top bin is open above: keep its lower edge
+        const float lo = __uint_as_float(tau);
+        const float hi = __uint_as_float((uint32_t)(kPBase + bin + 1) << kPShift);
+        const float f = (float)(want - b_above) / (float)b_cnt;  // in (0, 1]
+        tau = __float_as_uint(hi - f * (hi - lo));                // in [lo, hi]
       }
     }
   }
@@ -607,11 +625,20 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             tmem_ld32(taddr + (uint32_t)(32 * g), v);
             tmem_ld_wait();
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const float a0 = __uint_as_float(v[4 * kk]), a1 = __uint_as_float(v[4 * kk + 1]);
-              const float a2 = __uint_as_float(v[4 * kk + 2]), a3 = __uint_as_float(v[4 * kk + 3]);
-              u16[8 * g + kk] =
-                  __float_as_uint(((a0 + fabsf(a0)) + (a1 + fabsf(a1))) + ((a2 + fabsf(a2)) + (a3 + fabsf(a3))));
+            for (int kk = 0; kk < 8; kk += 2) {  // two tokens at a time: packed fp32 pair adds
+              float rr[2][4];
+#pragma unroll
+              for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) {
+                  const float a = __uint_as_float(v[4 * (kk + e) + hh]);
+                  rr[e][hh] = a + fabsf(a);
+                }
+              const float2 s01 = __fadd2_rn(make_float2(rr[0][0], rr[1][0]), make_float2(rr[0][1], rr[1][1]));
+              const float2 s23 = __fadd2_rn(make_float2(rr[0][2], rr[1][2]), make_float2(rr[0][3], rr[1][3]));
+              const float2 tot = __fadd2_rn(s01, s23);
+              u16[8 * g + kk] = __float_as_uint(tot.x);
+              u16[8 * g + kk + 1] = __float_as_uint(tot.y);
             }
           }
           tc_fence_before();
