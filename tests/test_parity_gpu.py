@@ -198,6 +198,30 @@ def test_planted_block_always_selected():
     QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, 4)
 
 
+def test_unsampled_high_blocks_take_the_exact_fallback():
+    """Rows that see 4096 blocks are pilot-sampled at block residues 0..11 (mod
+    16).  Here only blocks of residues 12..15 score high, so those rows'
+    thresholds come from the low scores, they collect more entries than their
+    buffer holds, and the exact full-row fallback must select them: the result
+    is still the oracle's."""
+    spec, wl = small_case(16384, 2048, seed=11)
+    cfg = cfg_for(spec)
+    g = torch.Generator(device="cpu").manual_seed(11)
+    d = torch.zeros(128)
+    d[64:] = torch.randn(64, generator=g)  # past the rotated dims: the same at every position
+    wl["q_idx"][:] = d.to(torch.bfloat16).to(DEV)  # every row and head
+    nb = spec.n // spec.r
+    high = (torch.arange(nb) % 16 >= 12).repeat_interleave(spec.r)
+    keys = 0.1 * torch.randn(spec.n, 128, generator=g)
+    keys[high] = 2 * d + 0.05 * torch.randn(int(high.sum()), 128, generator=g)
+    wl["k_idx"][0] = keys.to(torch.bfloat16).to(DEV)
+    gpu = run_prefill(cfg, wl)
+    rows = list(range(spec.n - 16, spec.n)) + [12295, 13000, 14000, 15000, 15500]
+    res = QC.oracle_rows(wl, rows, cfg=cfg)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, cfg.r)
+    assert st["exact"] >= len(rows) - 1, st
+
+
 def test_chunked_prefill_rows_at_offset():
     """A chunk of query rows at positions 1000.. against the whole cached prefix."""
     spec, wl = small_case(2048, 512, seed=12)
