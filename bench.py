@@ -567,6 +567,8 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "rooflines": roofs, "peaks_source": pk["source"],
         "gpu_launches": int(launches), "clocks": clk, "wall_s_timed": wall,
+        # rows of the last prefill that the indexer's exact full-row fallback selected
+        "index_fallback_rows": pre.fallback_rows(stream),
     }
 
     if not do_decode:

@@ -179,6 +179,21 @@ qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* 
   return QSA_OK;
 }
 
+qsa_status qsa_index_topk_fallback_rows(const qsa_config* cfg, int64_t B, int64_t n_q, int64_t n_blocks_max,
+                                        const void* ws, size_t ws_bytes, int64_t* rows, qsa_stream_t stream) {
+  qsa_status s = check_config(cfg);
+  if (s != QSA_OK) return s;
+  if (B < 0 || n_q < 0 || n_blocks_max < 0 || rows == nullptr) return QSA_ERR_INVALID_ARG;
+  *rows = 0;
+  if (B == 0 || n_q == 0) return QSA_OK;
+  const IndexLayout L = index_layout(B, n_q, n_blocks_max, k_blocks(cfg));
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return QSA_ERR_INVALID_ARG;
+  if (ws_bytes < L.total) return QSA_ERR_WORKSPACE;
+  if (!L.fused) return QSA_OK;  // the scan path selects every row exactly in one pass
+  return from_cuda(read_fused_fallback_rows(static_cast<const char*>(ws) + L.s_off, B, n_q, n_blocks_max, rows,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
 qsa_status qsa_sparse_attn_prefill(const qsa_config* cfg, const void* q, const void* k,
                                    const void* v, int64_t L_cap, const int64_t* q_pos,
                                    const int32_t* idx, const int32_t* count, int64_t B,

@@ -991,11 +991,19 @@ extern "C" int qsa_debug_fin_prof(unsigned long long* host, int reset) {
   }
   return 0;
 }
-extern "C" int qsa_debug_fallback_count(const void* ws, int64_t B, int64_t n_q, int64_t n_blocks_max, int* out) {
-  const FusedLayout L = fused_layout(B, n_q, n_blocks_max);
-  return cudaMemcpy(out, static_cast<const char*>(ws) + L.fb_count_off, sizeof(int), cudaMemcpyDeviceToHost) !=
-         cudaSuccess;
-}
 #endif
+
+// Rows of the last fused-indexer call on workspace `ws` (its fused part) that
+// went to the exact fallback kernel.  Waits for `st`.
+inline cudaError_t read_fused_fallback_rows(const void* ws, int64_t B, int64_t n_q, int64_t n_blocks_max,
+                                            int64_t* rows, cudaStream_t st) {
+  const FusedLayout L = fused_layout(B, n_q, n_blocks_max);
+  int n = 0;
+  cudaError_t e = cudaMemcpyAsync(&n, static_cast<const char*>(ws) + L.fb_count_off, sizeof(int),
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  *rows = n;
+  return e;
+}
 
 }  // namespace qsa

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED",
 
 EXPORTED = [
     "qsa_default_config", "qsa_num_selected_blocks", "qsa_compress_keys",
-    "qsa_index_topk_workspace", "qsa_index_topk", "qsa_sparse_attn_prefill",
+    "qsa_index_topk_workspace", "qsa_index_topk", "qsa_index_topk_fallback_rows", "qsa_sparse_attn_prefill",
     "qsa_sparse_attn_decode_workspace", "qsa_sparse_attn_decode", "qsa_sparse_attn_decode_noalloc",
     "qsa_sparse_attn_decode_multi_workspace", "qsa_sparse_attn_decode_multi",
     "qsa_probe_l2_gather", "qsa_selftest_wait_timeout", "qsa_status_string",
@@ -85,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qsa_compress_keys": (ctypes.c_int, [C, P, I64, I64, I64, I64, P, I64, P]),
         "qsa_index_topk_workspace": (SZ, [C, I64, I64, I64]),
         "qsa_index_topk": (ctypes.c_int, [C, P, P, I64, P, I64, I64, I64, P, P, P, SZ, P]),
+        "qsa_index_topk_fallback_rows": (ctypes.c_int, [C, I64, I64, I64, P, SZ, ctypes.POINTER(I64), P]),
         "qsa_sparse_attn_prefill": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I64, I32, I32, F, P, P, P]),
         "qsa_sparse_attn_decode_workspace": (SZ, [C, I64, I32, I32]),
         "qsa_sparse_attn_decode": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, F, P, P, P, SZ, P]),
@@ -165,6 +166,18 @@ def qsa_index_topk(cfg: Config, q_idx: torch.Tensor, kbar: torch.Tensor, q_pos: 
     _check("qsa_index_topk", load_library().qsa_index_topk(
         ctypes.byref(c), _ptr(q_idx), _ptr(kbar), kbar.stride(0), _ptr(q_pos), B, n_q, n_blocks_max,
         _ptr(idx), _ptr(count), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def qsa_index_topk_fallback_rows(cfg: Config, B: int, n_q: int, n_blocks_max: int, ws: torch.Tensor,
+                                 stream=None) -> int:
+    """Rows of the last qsa_index_topk call on `ws` (same sizes) that its exact
+    full-row fallback selected; waits for the stream."""
+    c = cfg.c_struct()
+    rows = ctypes.c_int64(0)
+    _check("qsa_index_topk_fallback_rows", load_library().qsa_index_topk_fallback_rows(
+        ctypes.byref(c), B, n_q, n_blocks_max, _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(rows),
+        _stream(stream)))
+    return int(rows.value)
 
 
 def qsa_sparse_attn_prefill(cfg: Config, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -313,6 +326,10 @@ class QsaPrefill:
         qsa_sparse_attn_prefill(self.cfg, q, k, v, self.q_pos, self.idx, self.count, self.out,
                                 self.lse if with_lse else None, stream=stream)
         return self.out
+
+    def fallback_rows(self, stream=None) -> int:
+        """Rows of the last call that the indexer's exact full-row fallback selected."""
+        return qsa_index_topk_fallback_rows(self.cfg, self.B, self.n, self.n_blocks, self.ws, stream)
 
 
 class QsaDecode:

@@ -135,6 +135,23 @@ qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* 
                           size_t ws_bytes, qsa_stream_t stream);
 
 /*
+ * Diagnostic for the prefill indexer: how many rows of the last qsa_index_topk
+ * call on `ws` (made with the same cfg, B, n_q, n_blocks_max) were selected by
+ * its exact full-row fallback.  The threshold pass collects the entries at or
+ * above a per-row threshold taken from a pilot sample; a row whose collection
+ * held fewer than k_B entries or more than its buffer (2.5 k_B) is scored again
+ * in full.  Its selection is exact either way; only its cost differs.  0 when
+ * that call took the one-pass scan path (fewer than 64 rows per sequence, or
+ * k_B > 512).  Waits for `stream` and copies one int to the host.
+ *   rows   host int64, written.
+ * QSA_ERR_INVALID_ARG for a NULL `rows` or workspace, QSA_ERR_WORKSPACE when
+ * ws_bytes is below qsa_index_topk_workspace for these sizes.
+ */
+qsa_status qsa_index_topk_fallback_rows(const qsa_config* cfg, int64_t B, int64_t n_q,
+                                        int64_t n_blocks_max, const void* ws, size_t ws_bytes,
+                                        int64_t* rows, qsa_stream_t stream);
+
+/*
  * Sparse core attention, prefill [QSA] step 5 and Fig. 3: for query row j of
  * sequence bb (token i = q_pos[bb] + j) and head h with kv head g = h / (Hq/Hkv),
  *   T_i   = union over selected b of [b*r, b*r + r)  plus the tail [c_i*r, i],

@@ -41,13 +41,14 @@ def run_prefill(cfg: qsa.Config, wl: dict, q_pos0: int = 0, rows: slice | None =
     cnt = torch.empty((B, n_q), dtype=torch.int32, device=DEV)
     ws = torch.empty((qsa.qsa_index_topk_workspace(cfg, B, n_q, nb),), dtype=torch.uint8, device=DEV)
     qsa.qsa_index_topk(cfg, q_idx, kbar, q_pos, nb, idx, cnt, ws)
+    fallback_rows = qsa.qsa_index_topk_fallback_rows(cfg, B, n_q, nb, ws)
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=DEV)
     qsa.qsa_sparse_attn_prefill(cfg, q, k, v, q_pos, idx, cnt, out, lse)
     torch.cuda.synchronize()
     assert qsa.qsa_read_device_error() == 0
     return {"kbar": kbar, "idx": idx.cpu().numpy(), "count": cnt.cpu().numpy(),
-            "out": out.float().cpu().numpy(), "lse": lse.cpu().numpy()}
+            "out": out.float().cpu().numpy(), "lse": lse.cpu().numpy(), "fallback_rows": fallback_rows}
 
 
 # ----------------------------------------------------------------------------- key compression
@@ -216,6 +217,7 @@ def test_unsampled_high_blocks_take_the_exact_fallback():
     keys[high] = 2 * d + 0.05 * torch.randn(int(high.sum()), 128, generator=g)
     wl["k_idx"][0] = keys.to(torch.bfloat16).to(DEV)
     gpu = run_prefill(cfg, wl)
+    assert gpu["fallback_rows"] > 0  # the path under test was taken
     rows = list(range(spec.n - 16, spec.n)) + [12295, 13000, 14000, 15000, 15500]
     res = QC.oracle_rows(wl, rows, cfg=cfg)
     st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, cfg.r)
