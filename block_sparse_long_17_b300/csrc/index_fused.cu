@@ -117,7 +117,7 @@ struct TileMeta {
 };
 
 constexpr int kPilotStride = 16;   // the pilot samples every 16th block (per phase)
-constexpr int kPilotMin = 3072;    // at least this many pilot samples per row when possible
+constexpr int kPilotMin = 2048;    // at least this many pilot samples per row when possible
 constexpr int kPilotNum = 8;       // tau aims at kPilotNum / kPilotDen x k_B entries per row:
 constexpr int kPilotDen = 5;       // near the middle, in ratio, of the accepted [k_B, 2.5 k_B]
 
