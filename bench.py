@@ -539,8 +539,9 @@ def main():
     roofs["index_prefill"]["frac_of_burst"] = roofs["index_prefill"]["achieved"] / pk["bf16_tflops"]
     roofs["index_prefill"]["frac_of_sustained"] = roofs["index_prefill"]["achieved"] / pk["bf16_tflops_sustained"]
     # The bound of prefill attention: gathering random 256-byte rows from a buffer
-    # the size of one kv head's K/V (resident in L2), measured on this GPU.
-    kv_bytes = 2 * pspec.n * pspec.d * 2
+    # the size of one kv head's K/V, capped at 64 MiB so that it stays resident
+    # in L2, measured on this GPU.
+    kv_bytes = min(2 * pspec.n * pspec.d * 2, 64 << 20)
     probe_buf = torch.empty((max(kv_bytes, 1 << 20) + 256,), dtype=torch.uint8, device=dev)
     probe_buf.fill_(1)
     l2_gather = qsa.qsa_probe_l2_gather(probe_buf)
