@@ -68,6 +68,15 @@ def peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
+def tensor_peak_for(clk: dict, pk: dict) -> tuple[float, str]:
+    """The bf16 tensor peak a kernel timed in these steps is held to: the burst
+    figure while the sampled clocks showed no power cap, the sustained
+    (power-capped) one when they did."""
+    if "sw_power_cap" in (clk.get("reasons") or []):
+        return pk["bf16_tflops_sustained"], "sustained"
+    return pk["bf16_tflops"], "burst"
+
+
 # ----------------------------------------------------------------------------- algorithmic work
 
 def prefill_work(n: int, r: int, k_b: int, hq: int, hkv: int, d: int = 128, h_idx: int = 4) -> dict:
@@ -514,12 +523,8 @@ def main():
     prefill_ms, decode_ms, step_ms = reduce_max_over_ranks([prefill_ms, decode_ms, step_ms], world, dev)
     value = job_tokens_per_s(world, pspec.n, prefill_ms)
 
-    # Roofline of each part (algorithmic work / measured mean duration).  The
-    # tensor peak is the burst figure while the clocks stayed free of the power
-    # cap during the timed steps, the sustained (power-capped) one otherwise.
-    capped = "sw_power_cap" in (clk.get("reasons") or [])
-    tensor_peak = pk["bf16_tflops_sustained"] if capped else pk["bf16_tflops"]
-    tensor_peak_kind = "sustained" if capped else "burst"
+    # Roofline of each part (algorithmic work / measured mean duration).
+    tensor_peak, tensor_peak_kind = tensor_peak_for(clk, pk)
     pw = prefill_work(pspec.n, pspec.r, pspec.k_b, pspec.hq, pspec.hkv)
     dwk = decode_work(dspec.batch, dwl["cache_len"], dspec.r, dspec.k_b, dspec.hq, dspec.hkv)
     hbm = pk["hbm_gbs"]

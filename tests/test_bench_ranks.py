@@ -50,3 +50,12 @@ def test_two_rank_max_and_weak_scaling_value():
 def test_single_rank_passes_values_through():
     assert bench.reduce_max_over_ranks([1.5, 2.5], 1, "cpu") == [1.5, 2.5]
     assert bench.job_tokens_per_s(1, 1000, 2.0) == pytest.approx(500000.0)
+
+
+def test_tensor_peak_follows_the_clock_record():
+    """The indexer's roofline denominator: the burst bf16 peak while the sampled
+    clocks show no power cap, the sustained one when they do."""
+    pk = {"bf16_tflops": 1755.6, "bf16_tflops_sustained": 1373.1}
+    assert bench.tensor_peak_for({"reasons": []}, pk) == (1755.6, "burst")
+    assert bench.tensor_peak_for({"reasons": ["sw_power_cap"]}, pk) == (1373.1, "sustained")
+    assert bench.tensor_peak_for({"reasons": ["nvidia-smi unavailable"]}, pk) == (1755.6, "burst")
