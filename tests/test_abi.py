@@ -113,3 +113,22 @@ def test_workspace_sizes_and_checks(lib):
     assert wd > 0 and wd % 256 == 0
     assert lib.qsa_sparse_attn_decode(ctypes.byref(c), fake, fake, fake, 16, fake, fake, fake, 64, 16, 2,
                                       0.1, fake, None, fake, wd - 1, None) == 3
+
+
+def test_fallback_rows_checks_before_any_cuda_call(lib):
+    c = _cfg()
+    fake = ctypes.c_void_p(256)
+    rows = ctypes.c_int64(-7)
+    ws = lib.qsa_index_topk_workspace(ctypes.byref(c), 1, 2048, 512)
+    # no output pointer, or too small a workspace: rejected on the host
+    assert lib.qsa_index_topk_fallback_rows(ctypes.byref(c), 1, 2048, 512, fake, ws, None, None) == 1
+    assert lib.qsa_index_topk_fallback_rows(ctypes.byref(c), 1, 2048, 512, fake, ws - 1,
+                                            ctypes.byref(rows), None) == 3
+    # empty work and the one-pass scan path (fewer than 64 rows) report 0 without a launch
+    assert lib.qsa_index_topk_fallback_rows(ctypes.byref(c), 1, 0, 512, None, 0, ctypes.byref(rows), None) == 0
+    assert rows.value == 0
+    rows.value = -7
+    ws_scan = lib.qsa_index_topk_workspace(ctypes.byref(c), 1, 4, 512)
+    assert lib.qsa_index_topk_fallback_rows(ctypes.byref(c), 1, 4, 512, fake, ws_scan,
+                                            ctypes.byref(rows), None) == 0
+    assert rows.value == 0
