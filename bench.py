@@ -385,7 +385,8 @@ def oracle_timing(pre_spec, dec_spec, rows_per_step: int, steps: int, seed: int 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 20; the CPU reference arm: 5)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["qsa", "reference"], default="qsa")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -398,6 +399,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the chunked-prefill and dense-decode lines timed after the main step")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 5 if args.impl == "reference" else 20
 
     import torch
     from block_sparse_long_17_b300.workloads import WORKLOADS
@@ -518,6 +521,9 @@ def main():
             parts[nm].append(evs[j].elapsed_time(evs[j + 1]))
     mean = {nm: statistics.mean(v) for nm, v in parts.items()}
     prefill_ms = mean["compress"] + mean["index_prefill"] + mean["attn_prefill"]
+    prefill_each = [parts["compress"][j] + parts["index_prefill"][j] + parts["attn_prefill"][j]
+                    for j in range(len(all_evs))]
+    decode_each = [parts["index_decode"][j] + parts["attn_decode"][j] for j in range(len(all_evs))]
     decode_ms = mean["index_decode"] + mean["attn_decode"]
     step_ms = prefill_ms + decode_ms
     prefill_ms, decode_ms, step_ms = reduce_max_over_ranks([prefill_ms, decode_ms, step_ms], world, dev)
@@ -564,6 +570,9 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "decode_us_per_step": decode_ms * 1e3,
         "prefill_ms": prefill_ms,
+        # medians over the timed steps (the value above uses the means)
+        "prefill_ms_median": statistics.median(prefill_each),
+        "decode_us_median": statistics.median(decode_each) * 1e3 if do_decode else None,
         "parts_ms": mean,
         "config": {"workload": f"{pspec.name} + {dspec.name if do_decode else 'no decode'}",
                    "prefill_tokens": pspec.n, "prefill_batch": 1,
