@@ -262,7 +262,7 @@ def dense_prefill_measure(wl, qsa_prefill_ms: float, steps: int, warmup: int, fl
                 torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True, enable_gqa=True)
 
         ms = _median_step_ms(step, min(steps, 5), warmup, flush)
-    except Exception as ex:  # no fused dense backend on this build: report it instead
+    except Exception as ex:  # PyTorch offers no fused dense backend here: report it instead
         return {"unavailable": str(ex).split("\n")[0][:160]}
     n, hq, d = q.shape[2], q.shape[1], q.shape[3]
     flops = 4 * hq * d * n * (n + 1) / 2
