@@ -21,7 +21,10 @@
  *     never allocates device memory; scratch space is the caller's workspace
  *     (`ws`, `ws_bytes`), whose required size the matching *_workspace() call
  *     returns.  Workspace pointers must be 256-byte aligned.
- *   - Every call is ordered on `stream` and returns without synchronising.
+ *   - Every call is ordered on `stream` and returns without synchronising,
+ *     except the three that read a value back to the host
+ *     (qsa_index_topk_fallback_rows, qsa_probe_l2_gather, qsa_read_device_error),
+ *     which synchronise `stream` first.
  *   - Arguments are checked on the host before any launch.  A bad argument
  *     returns QSA_ERR_INVALID_ARG and launches nothing; a shape outside what the
  *     kernels are built for returns QSA_ERR_UNSUPPORTED; a launch failure returns
