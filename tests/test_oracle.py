@@ -298,3 +298,101 @@ def test_decode_equals_last_prefill_row():
     dec = O.decode_rows(q_idx[L - 1], q[L - 1], kbar, k, v, L, r=r, k_tokens=64)
     np.testing.assert_array_equal(dec["sel"][0], pre["sel"][0])
     np.testing.assert_array_equal(dec["out"], pre["out"])
+
+
+# ------------------------------------------------------------------ query rotation and k_B
+# The query-side reading (research-hub notes, "Key ideas", QSA bullet: partial
+# RoPE after compression; keys sit at block index b, so query token i sits at
+# the index floor(i / r) of the block it lies in, and the rotated query is
+# stored in bf16).  Each pin below is computed without the oracle's own rotation
+# routine: complex multiplication for the rotation, torch for the bf16 rounding.
+
+def _complex_rope(x: np.ndarray, angle_pos: float, base: float = 10000.0) -> np.ndarray:
+    """Rotate dims 0..63 of x by pos * base^(-j/32) as complex numbers x_j + i x_{j+32}."""
+    theta = base ** (-np.arange(32) / 32.0)
+    z = (x[..., :32] + 1j * x[..., 32:64]) * np.exp(1j * angle_pos * theta)
+    out = np.array(x, dtype=np.float64, copy=True)
+    out[..., :32] = z.real
+    out[..., 32:64] = z.imag
+    return out
+
+
+def _torch_bf16(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.asarray(x, np.float64)).to(torch.bfloat16).double().numpy()
+
+
+def test_rotate_queries_is_rounded_rotation_at_block_index():
+    """Each rotated query is the rotation at floor(i / r), rounded once to bf16."""
+    rng = np.random.default_rng(20)
+    r = 4
+    positions = np.array([0, 1, 3, 4, 7, 9, 130, 131, 4097, 262143])
+    q = O.round_to_bf16(rng.standard_normal((len(positions), 4, 128)))  # bf16 inputs, as the library gets
+    got = O.rotate_queries(q, positions, r)
+    assert got.shape == q.shape
+    np.testing.assert_array_equal(O.round_to_bf16(got), got)  # stored as bf16 numbers
+    for n, i in enumerate(positions):
+        ref = _torch_bf16(_complex_rope(q[n], i // r))
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7)
+        assert np.all(np.abs(got[n] - ref) <= ulp), i  # fp64 rotation order may flip a halfway case
+        assert (got[n] == ref).mean() > 0.99, i
+        np.testing.assert_array_equal(got[n][:, 64:], q[n][:, 64:])  # unrotated dims pass through
+
+
+def test_rotate_queries_hand_cases():
+    # Dim 0 rotates at theta_0 = 1 rad per block: token 9 with r = 4 is in block 2.
+    q = np.zeros((1, 4, 128))
+    q[0, :, 0] = 1.0
+    got = O.rotate_queries(q, [9], 4)
+    assert got[0, 0, 0] == _torch_bf16(math.cos(2.0)) and got[0, 0, 32] == _torch_bf16(math.sin(2.0))
+    assert got[0, 0, 0] == -0.416015625 and got[0, 0, 32] == 0.91015625  # bf16(cos 2), bf16(sin 2)
+    assert np.count_nonzero(got[0]) == 8
+    # A base with theta_16 = pi / 2: token 6 with r = 4 (block 1) turns dim 16 onto
+    # dim 48; at position 6 (the token index) it would land on -dim 16, and with
+    # the sign of the angle flipped on -dim 48.
+    base = (2.0 / math.pi) ** 2
+    q = np.zeros((1, 1, 128))
+    q[0, 0, 16] = 1.0
+    got = O.rotate_queries(q, [6], 4, rope_base=base)[0, 0]
+    assert got[48] == 1.0
+    assert abs(got[16]) < 1e-15
+    assert np.count_nonzero(np.abs(got) > 1e-15) == 1
+
+
+def test_indexer_score_depends_on_block_distance_only():
+    """<qt_i, kbar_b> equals <q, R_(b - floor(i/r)) pooled_b> for every token i of a
+    block and every block b it sees, within the bf16 storage bound; when token i
+    closes its own block b (b = floor(i/r)) the rotations cancel and the product
+    is the unrotated one."""
+    rng = np.random.default_rng(21)
+    r, n = 4, 64
+    k = O.round_to_bf16(rng.standard_normal((n, 128)))
+    pooled = k.reshape(n // r, r, 128).mean(axis=1)
+    kbar = O.compress_keys(k, r)
+    q = rng.standard_normal((1, 4, 128))
+    for i in range(36, 40):  # the four tokens of block 9
+        p = i // r
+        assert p == 9
+        qt = O.rotate_queries(q, [i], r)[0]
+        for b in range(O.visible_blocks(i, r)):
+            rel = _complex_rope(pooled[b], b - p)
+            want = rel @ q[0].T  # [4 heads]
+            got = kbar[b] @ qt.T
+            # q and kbar each carry one bf16 rounding (relative 2^-9 per element).
+            bound = 2.0 ** -8 * (np.abs(q[0]) @ np.abs(rel)) * 1.01
+            assert np.all(np.abs(got - want) <= bound), (i, b)
+        if i == 39:  # token 39 closes block 9, which it now sees
+            own = kbar[9] @ qt.T
+            bound = 2.0 ** -8 * (np.abs(q[0]) @ np.abs(pooled[9])) * 1.01
+            assert np.all(np.abs(own - q[0] @ pooled[9]) <= bound)
+
+
+def test_n_select_is_a_ceiling():
+    assert O.n_select(2048, 4) == 512
+    assert O.n_select(2049, 4) == 513
+    assert O.n_select(6, 4) == 2
+    assert O.n_select(1, 16) == 1
+    assert O.n_select(512, 4) == 128
+    for K in range(1, 70):
+        for r in (1, 2, 4, 8, 16):
+            kb = O.n_select(K, r)
+            assert (kb - 1) * r < K <= kb * r
