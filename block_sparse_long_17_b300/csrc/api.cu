@@ -2,7 +2,6 @@
 // kernel dispatch.  The kernel sources are compiled into this one translation
 // unit so that they share the device error word without relocatable device code.
 #include <cmath>
-#include <cstdio>
 
 #include "common.cuh"
 
@@ -44,6 +43,12 @@ qsa_status check_config(const qsa_config* c) {
 
 int k_blocks(const qsa_config* c) { return (c->k_tokens + c->r - 1) / c->r; }
 
+// Softmax scale of the attention calls: a caller value <= 0 selects the usual
+// 1 / sqrt(head_dim).
+float softmax_scale(const qsa_config* c, float scale) {
+  return scale > 0.f ? scale : (float)(1.0 / std::sqrt((double)c->head_dim));
+}
+
 RopeParams rope_params(const qsa_config* c) {
   RopeParams p{};
   p.half = c->rope_dims / 2;
@@ -52,11 +57,7 @@ RopeParams rope_params(const qsa_config* c) {
   return p;
 }
 
-qsa_status from_cuda(cudaError_t e) {
-  if (e == cudaSuccess) return QSA_OK;
-  std::fprintf(stderr, "qsa: CUDA error %s\n", cudaGetErrorString(e));
-  return QSA_ERR_CUDA;
-}
+qsa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSA_OK : QSA_ERR_CUDA; }
 
 struct IndexLayout {
   bool fused;
@@ -209,7 +210,7 @@ qsa_status qsa_sparse_attn_prefill(const qsa_config* cfg, const void* q, const v
   return from_cuda(launch_sparse_attn_prefill(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
       static_cast<const __nv_bfloat16*>(v), L_cap, q_pos, idx, count, B, n_q, Hq, Hkv, cfg->r,
-      k_blocks(cfg), scale, static_cast<__nv_bfloat16*>(out), lse,
+      k_blocks(cfg), softmax_scale(cfg, scale), static_cast<__nv_bfloat16*>(out), lse,
       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -237,7 +238,7 @@ qsa_status qsa_sparse_attn_decode(const qsa_config* cfg, const void* q, const vo
   return from_cuda(launch_sparse_attn_decode(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_cache),
       static_cast<const __nv_bfloat16*>(v_cache), L_cap, cache_len, idx, count, B, 1, Hq, Hkv,
-      cfg->r, k_blocks(cfg), scale, static_cast<__nv_bfloat16*>(out), lse, ws,
+      cfg->r, k_blocks(cfg), softmax_scale(cfg, scale), static_cast<__nv_bfloat16*>(out), lse, ws,
       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -266,7 +267,7 @@ qsa_status qsa_sparse_attn_decode_multi(const qsa_config* cfg, const void* q, co
   return from_cuda(launch_sparse_attn_decode(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_cache),
       static_cast<const __nv_bfloat16*>(v_cache), L_cap, cache_len, idx, count, B, n_q, Hq, Hkv,
-      cfg->r, k_blocks(cfg), scale, static_cast<__nv_bfloat16*>(out), lse, ws,
+      cfg->r, k_blocks(cfg), softmax_scale(cfg, scale), static_cast<__nv_bfloat16*>(out), lse, ws,
       reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -305,9 +306,6 @@ const char* qsa_version(void) { return "qsa-b300 0.1 sm_103a"; }
 
 // Decode entry point with library-owned static scratch (no allocation).
 #include "decode_noalloc.cu"
-
-// Measurement helper for the attention roofline.
-#include "probe.cu"
 
 // Diagnostic entry point for the bounded-wait path.
 #include "selftest.cu"

@@ -13,56 +13,71 @@ namespace qsa {
 
 constexpr int kCompressWarps = 8;
 
-// One warp per compressed block.  Lane l owns dims {l, l+32, l+64, l+96} while
-// pooling; the pooled fp32 row is staged in shared memory so that any even
-// rope_dims can pair dim j with dim j + rope_dims/2.
+// One warp per compressed block.  Pooling reads the block's r rows with
+// 16-byte loads: lane l takes dims 8 (l % 16) .. + 7 of the rows t = l / 16,
+// l / 16 + 2, ..., and the two half-warps add their sums.  The pooled fp32 row
+// is staged in shared memory so that any even rope_dims can pair dim j with
+// dim j + rope_dims/2; lane l then rotates and stores dims 4 l .. 4 l + 3
+// (one 256-byte store per warp).
 __global__ void __launch_bounds__(kCompressWarps * 32)
 compress_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_t k_stride_b, int64_t B,
                      int64_t first_block, int64_t n_blocks, int r, int rmsnorm, float rms_eps,
                      RopeParams rope, __nv_bfloat16* __restrict__ kbar, int64_t kbar_stride_b) {
-  __shared__ float pooled[kCompressWarps][kHeadDim];
+  __shared__ __align__(16) float pooled[kCompressWarps][kHeadDim];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t item = (int64_t)blockIdx.x * kCompressWarps + warp;
   if (item >= B * n_blocks) return;
   const int64_t bb = item / n_blocks;
   const int64_t blk = first_block + item % n_blocks;
   const __nv_bfloat16* src = k_idx + bb * k_stride_b + blk * r * kHeadDim;
+  const int chunk = lane & 15;
 
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int t = 0; t < r; ++t) {
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int t = lane >> 4; t < r; t += 2) {
+    const uint4 v = ldg_stream(src + t * kHeadDim + 8 * chunk);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[u] += __bfloat162float(src[t * kHeadDim + lane + 32 * u]);
+    for (int u = 0; u < 4; ++u) {
+      acc[2 * u] += bf16_lo(w[u]);
+      acc[2 * u + 1] += bf16_hi(w[u]);
+    }
   }
   const float inv_r = 1.0f / (float)r;  // r is a power of two: exact
 #pragma unroll
-  for (int u = 0; u < 4; ++u) acc[u] *= inv_r;
-  if (rmsnorm) {
-    float ss = acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3];
+  for (int u = 0; u < 8; ++u) acc[u] = (acc[u] + __shfl_xor_sync(0xffffffffu, acc[u], 16)) * inv_r;
+  if (rmsnorm) {  // both half-warps hold the whole row: reduce over 16 lanes
+    float ss = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    for (int u = 0; u < 8; ++u) ss += acc[u] * acc[u];
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float inv = rsqrtf(ss * (1.0f / kHeadDim) + rms_eps);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) acc[u] *= inv;
+    for (int u = 0; u < 8; ++u) acc[u] *= inv;
   }
-#pragma unroll
-  for (int u = 0; u < 4; ++u) pooled[warp][lane + 32 * u] = acc[u];
+  if (lane < 16) {
+    float4* dstp = reinterpret_cast<float4*>(&pooled[warp][8 * chunk]);
+    dstp[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dstp[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
   __syncwarp();
 
-  __nv_bfloat16* dst = kbar + bb * kbar_stride_b + blk * kHeadDim;
   const int half = rope.half;
+  float y[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    const int dim = lane + 32 * u;
-    float y = pooled[warp][dim];
+    const int dim = 4 * lane + u;
+    y[u] = pooled[warp][dim];
     if (dim < 2 * half) {
       const int j = dim < half ? dim : dim - half;
       float c, s;
       rope_cos_sin(blk, rope.theta[j], &c, &s);
       const float x1 = pooled[warp][j], x2 = pooled[warp][j + half];
-      y = dim < half ? fmaf(x1, c, -x2 * s) : fmaf(x1, s, x2 * c);
+      y[u] = dim < half ? fmaf(x1, c, -x2 * s) : fmaf(x1, s, x2 * c);
     }
-    dst[dim] = __float2bfloat16_rn(y);
   }
+  __nv_bfloat16* dst = kbar + bb * kbar_stride_b + blk * kHeadDim;
+  *reinterpret_cast<uint2*>(dst + 4 * lane) = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
 }
 
 // One warp per query token: the RoPE angles of position floor(i / r) are

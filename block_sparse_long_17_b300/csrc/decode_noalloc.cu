@@ -31,28 +31,39 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 namespace {
 
-struct NoAllocSlot {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
-};
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
 
-NoAllocSlot g_noalloc_slots[kNoAllocMaxDevices];
-
-// Device address of the scratch array on the current device (looked up once).
-cudaError_t noalloc_scratch_ptr(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+// Device address of the scratch array on device `dev`, which must be the
+// current device.  Only a successful lookup is kept: after a failed one (say,
+// inside a stream capture, or with an error pending) the next call tries again.
+cudaError_t noalloc_scratch_ptr(int dev, void** out) {
   if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
-  NoAllocSlot& s = g_noalloc_slots[dev];
-  std::call_once(s.once, [&s]() {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
     void* p = nullptr;
-    s.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    s.ptr = (s.err == cudaSuccess) ? p : nullptr;
-  });
-  *out = s.ptr;
-  return s.err;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+// The scratch address is per device, so the stream and the query tensor must
+// both belong to the current device.
+bool on_current_device(int dev, const void* q, cudaStream_t st) {
+  int sdev = -1;
+  if (cudaStreamGetDevice(st, &sdev) != cudaSuccess || sdev != dev) {
+    cudaGetLastError();  // a failed query leaves no sticky error behind
+    return false;
+  }
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, q) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
 }
 
 }  // namespace
@@ -66,20 +77,19 @@ extern "C" qsa_status qsa_sparse_attn_decode_noalloc(const qsa_config* cfg, cons
                                                      void* out, float* lse, qsa_stream_t stream) {
   using namespace qsa;
   const size_t need = qsa_sparse_attn_decode_workspace(cfg, B, Hq, Hkv);
-  if (B > 0 && need == 0) {
-    // Invalid arguments: let the regular entry point report which status applies.
+  if (B <= 0 || need == 0) {
+    // No work, or invalid arguments: the regular entry point reports the status
+    // that applies (it returns before touching the missing workspace).
     return qsa_sparse_attn_decode(cfg, q, k_cache, v_cache, L_cap, cache_len, idx, count, B, Hq,
                                   Hkv, scale, out, lse, nullptr, 0, stream);
   }
-  if (need > kNoAllocScratchBytes) {
-    std::fprintf(stderr,
-                 "qsa_sparse_attn_decode_noalloc: this batch needs %zu bytes of scratch, above the "
-                 "fixed %zu; use qsa_sparse_attn_decode with a workspace or split the batch\n",
-                 need, kNoAllocScratchBytes);
-    return QSA_ERR_WORKSPACE;
-  }
+  if (need > kNoAllocScratchBytes) return QSA_ERR_WORKSPACE;  // beyond the fixed scratch
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (q == nullptr || !on_current_device(dev, q, reinterpret_cast<cudaStream_t>(stream))) return QSA_ERR_INVALID_ARG;
   void* scratch = nullptr;
-  cudaError_t e = noalloc_scratch_ptr(&scratch);
+  e = noalloc_scratch_ptr(dev, &scratch);
   if (e != cudaSuccess) return from_cuda(e);
   return qsa_sparse_attn_decode(cfg, q, k_cache, v_cache, L_cap, cache_len, idx, count, B, Hq, Hkv,
                                 scale, out, lse, scratch, kNoAllocScratchBytes, stream);

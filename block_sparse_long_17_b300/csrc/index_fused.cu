@@ -75,22 +75,6 @@ constexpr int kFinKWarps = 4;            // warps per CTA of the finalize kernel
 constexpr uint32_t kABytes = kMB * 128 * 2;     // 32 KB
 constexpr uint32_t kBBytes = kNRows * 128 * 2;  // 48 KB
 
-// Optional per-role cycle counters for tuning builds (-DQSA_FUSED_PROF).
-#ifdef QSA_FUSED_PROF
-__device__ unsigned long long g_fused_prof[kFMaxCtas][16];
-#define FPROF_T0(name) const long long name = clock64()
-#define FPROF_ADD(slot, t0) atomicAdd(&g_fused_prof[blockIdx.x][slot], (unsigned long long)(clock64() - (t0)))
-#define FPROF_CNT(slot, v) atomicAdd(&g_fused_prof[blockIdx.x][slot], (unsigned long long)(v))
-__device__ unsigned long long g_fin_prof[kFMaxCtas][8];
-#define FINPROF_ADD(slot, t0) \
-  if ((threadIdx.x & 31) == 0) atomicAdd(&g_fin_prof[blockIdx.x % kFMaxCtas][slot], (unsigned long long)(clock64() - (t0)))
-#else
-#define FINPROF_ADD(slot, t0)
-#define FPROF_T0(name)
-#define FPROF_ADD(slot, t0)
-#define FPROF_CNT(slot, v)
-#endif
-
 struct FusedSmem {
   uint8_t a[kAStages][2][kMB * 128];   // kbar chunk, dims 0-63 | 64-127 (SW128)
   uint8_t b[2][kNRows * 128];          // rotated queries of the tile, same split
@@ -232,7 +216,6 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
                                              int k_b, uint32_t* __restrict__ hist,
                                              int32_t* __restrict__ ids, int32_t* __restrict__ out) {
   const int lane = threadIdx.x & 31;
-  FPROF_T0(f0);
   uint32_t ru[kFinRegs];
 #pragma unroll
   for (int j0 = 0; j0 < kFinRegs; j0 += 16) {  // up to 16 loads in flight per lane
@@ -266,8 +249,6 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
     lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
     hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
-  FINPROF_ADD(0, f0);
-  FPROF_T0(f1);
   int need = k_b, mode = (lo == hi) ? 2 : 0;
   for (int guard = 0; mode == 0 && guard < 6; ++guard) {  // the range shrinks 2^9-fold per round
     const int shift = range_shift(lo, hi);
@@ -278,13 +259,8 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
     for (int j = 0; j < kFinRegs; ++j)
       if (lane + 32 * j < n && ru[j] >= lo && ru[j] <= hi) atomicAdd(&hist[(ru[j] - lo) >> shift], 1u);
     refine_round(hist, lo, hi, need, mode, shift);
-#ifdef QSA_FUSED_PROF
-    if (lane == 0) atomicAdd(&g_fin_prof[blockIdx.x % kFMaxCtas][6], 1ull);
-#endif
   }
   __syncwarp();
-  FINPROF_ADD(1, f1);
-  FPROF_T0(f2);
   // Ties at a single value: keep the `need` lowest block ids among them.
   uint32_t tie_cut = 0xffffffffu;  // tied entries with block id < tie_cut win
   if (mode == 2) {
@@ -317,8 +293,6 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
       tie_cut = 0x7fffffffu - blo + 1u;
     }
   }
-  FINPROF_ADD(2, f2);
-  FPROF_T0(f3);
   // Entry order is block order, so compacting the k_b winners in entry order
   // lists them sorted.
   int written = 0;
@@ -338,10 +312,6 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
   }
   for (int i = (written < k_b ? written : k_b) + lane; i < k_b; i += 32) out[i] = -1;
   __syncwarp();
-  FINPROF_ADD(3, f3);
-#ifdef QSA_FUSED_PROF
-  if (lane == 0) atomicAdd(&g_fin_prof[blockIdx.x % kFMaxCtas][7], 1ull);
-#endif
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -429,7 +399,6 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &S.abort_flag;
   const int64_t rounds = (t_count + gridDim.x - 1) / gridDim.x;
-  FPROF_T0(t_kernel);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
@@ -526,9 +495,7 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           const int st = it % kAStages;
           const int acc = ct & 1;
           if (!mbar_wait(&S.a_full[st], (it / kAStages) & 1, abort_flag, kWaitCycles, 32)) { ok = false; break; }
-          FPROF_T0(t2);
           if (!mbar_wait(&S.tempty[acc], ((ct >> 1) & 1) ^ 1, abort_flag, kWaitCycles, 32)) { ok = false; break; }
-          FPROF_ADD(3, t2);
           tc_fence_after();
           const uint32_t a0 = smem_u32(S.a[st][0]), a1 = smem_u32(S.a[st][1]);
           const uint32_t d = tmem + (uint32_t)acc * kAccCols;
@@ -578,7 +545,6 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         const bool pilot = x < m.npilot;
         if (x == m.npilot) {
           // ---- pilot done: thresholds of tokens ew, ew + kEpiWarps, ...
-          FPROF_T0(tt0);
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.pilot_bar);
           if (!warp_wait(&S.pilot_bar, pilot_n & 1, abort_flag)) { ok = false; break; }
@@ -600,14 +566,10 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             tau16[4 * k4 + 2] = t4.z;
             tau16[4 * k4 + 3] = t4.w;
           }
-          if (ew == 0 && lane == 0) FPROF_ADD(8, tt0);
           ++pilot_n;
         }
         const int acc = ct & 1;
-        FPROF_T0(ts);
         if (!warp_wait(&S.tfull[acc], (ct >> 1) & 1, abort_flag)) { ok = false; break; }
-        if (ew == 0 && lane == 0) { FPROF_ADD(5, ts); FPROF_CNT(12, 1); }
-        FPROF_T0(tp);
         tc_fence_after();
 
         // The 64 accumulator columns of this warp's 16 tokens are reduced to
@@ -616,7 +578,6 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         // doubling commutes with the rounding of the sums, so the bit patterns
         // of 2 x score order exactly as the scores do.
         uint32_t u16[16];
-        FPROF_T0(tl);
         {
           const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)acc * kAccCols + (uint32_t)(64 * h);
 #pragma unroll
@@ -645,8 +606,6 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.tempty[acc]);
         }
-        if (ew == 0 && lane == 0) FPROF_ADD(14, tl);
-        FPROF_T0(tc);
         // Blocks of this warp's lanes: main chunk ch holds blocks gbase + lane,
         // gbase = q4 R + 32 ch (the quarter's own region of R = 32 nchunks
         // blocks); pilot chunks hold blocks 16 (gbase + lane) + ph, gbase = kMB kc + 32 q4.
@@ -705,7 +664,6 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             }
           }
         }
-        if (ew == 0 && lane == 0) { FPROF_ADD(6, tp); FPROF_ADD(pilot ? 1 : 15, tc); FPROF_CNT(pilot ? 0 : 13, 1); }
       }
       if (!ok) break;
       // ---- tile done: this warp's entry counts go to the finalize kernel
@@ -721,7 +679,6 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) FPROF_ADD(11, t_kernel);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -931,12 +888,9 @@ cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kba
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(index_topk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kFusedSmemBytes);
+  {
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(index_topk_fused_kernel), (int)kFusedSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   int* fb_count = reinterpret_cast<int*>(w + L.fb_count_off);
   int64_t* fb_rows = reinterpret_cast<int64_t*>(w + L.fb_rows_off);
@@ -944,10 +898,8 @@ cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kba
   int* cnt = reinterpret_cast<int*>(w + L.cnt_off);
   cudaError_t e = cudaMemsetAsync(fb_count, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
   int rshift = 0;  // r is a power of two
   while ((1 << rshift) < r) ++rshift;
@@ -974,24 +926,6 @@ cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kba
   return count_launch(cudaGetLastError());
 }
 
-#ifdef QSA_FUSED_PROF
-extern "C" int qsa_debug_fused_prof(unsigned long long* host, int reset) {
-  if (cudaMemcpyFromSymbol(host, g_fused_prof, sizeof(g_fused_prof)) != cudaSuccess) return 1;
-  if (reset) {
-    static unsigned long long zeros[kFMaxCtas][16] = {};
-    if (cudaMemcpyToSymbol(g_fused_prof, zeros, sizeof(zeros)) != cudaSuccess) return 1;
-  }
-  return 0;
-}
-extern "C" int qsa_debug_fin_prof(unsigned long long* host, int reset) {
-  if (cudaMemcpyFromSymbol(host, g_fin_prof, sizeof(g_fin_prof)) != cudaSuccess) return 1;
-  if (reset) {
-    static unsigned long long zeros[kFMaxCtas][8] = {};
-    if (cudaMemcpyToSymbol(g_fin_prof, zeros, sizeof(zeros)) != cudaSuccess) return 1;
-  }
-  return 0;
-}
-#endif
 
 // Rows of the last fused-indexer call on workspace `ws` (its fused part) that
 // went to the exact fallback kernel.  Waits for `st`.

@@ -231,17 +231,12 @@ template <int NT>
 static cudaError_t launch_decode_scan_nt(const __nv_bfloat16* qt, const __nv_bfloat16* kbar, int64_t kbar_stride_b,
                                          const int64_t* q_pos, int64_t B, int n_q, int r, int64_t c_max, float* S,
                                          int64_t s_stride, cudaStream_t st) {
-  static int blocks_per_sm = 0;
-  if (blocks_per_sm == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, decode_scan_kernel<NT>,
-                                                                  kScanWarps * 32, 0);
-    if (e != cudaSuccess) return e;
-    if (blocks_per_sm < 1) blocks_per_sm = 1;
-  }
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  int blocks_per_sm = 0, sms = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, decode_scan_kernel<NT>,
+                                                                kScanWarps * 32, 0);
   if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (blocks_per_sm < 1) blocks_per_sm = 1;
+  e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
   const int64_t tiles_per_seq = (c_max + 15) / 16;
   const int64_t total = B * tiles_per_seq;

@@ -327,9 +327,14 @@ __device__ void combine_unit(const float* __restrict__ po_unit, const float* __r
       x[h] = __ldcg(reinterpret_cast<const float4*>(po_unit + (sp * 8 + h) * kHeadDim) + lane);
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
-      const float w = ms[h] > -INFINITY ? exp2f(ms[h] - mmax[h]) : 0.f;
-      L[h] += w * ls[h];
-      acc[h].x += w * x[h].x; acc[h].y += w * x[h].y; acc[h].z += w * x[h].z; acc[h].w += w * x[h].w;
+      // An empty split stores max = -inf and never writes its partial output,
+      // so whatever an earlier call left there (possibly Inf or NaN) must not
+      // enter the sum, not even multiplied by a zero weight.
+      if (ms[h] > -INFINITY) {
+        const float w = exp2f(ms[h] - mmax[h]);
+        L[h] += w * ls[h];
+        acc[h].x += w * x[h].x; acc[h].y += w * x[h].y; acc[h].z += w * x[h].z; acc[h].w += w * x[h].w;
+      }
     }
   }
 #pragma unroll
@@ -434,19 +439,13 @@ size_t decode_workspace_bytes(int64_t B, int Hq, int Hkv, int k_b, int r) {
   return (parts + 255) / 256 * 256 + (size_t)units * sizeof(int);
 }
 
-// Grid of a persistent attention kernel (<= one CTA per SM); sets the kernel's
-// dynamic shared memory limit on first use.
-static cudaError_t attn_grid(const void* kernel, int which, int64_t items, int* grid) {
-  static bool attr_done[2] = {false, false};
-  if (!attr_done[which]) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kASmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done[which] = true;
-  }
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+// Grid of a persistent attention kernel (<= one CTA per SM); raises the
+// kernel's dynamic shared memory limit on the current device first.
+static cudaError_t attn_grid(const void* kernel, int64_t items, int* grid) {
+  cudaError_t e = ensure_dyn_smem(kernel, kASmemBytes);
   if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
   const int64_t need = (items + kAWarps - 1) / kAWarps;
   *grid = (int)(need < sms ? need : sms);
@@ -462,7 +461,7 @@ cudaError_t launch_sparse_attn_prefill(const __nv_bfloat16* q, const __nv_bfloat
   const int64_t items = B * n_q * Hkv * n_hc;
   if (items == 0) return cudaSuccess;
   int grid = 0;
-  cudaError_t e = attn_grid(reinterpret_cast<const void*>(sparse_attn_prefill_kernel), 0, items, &grid);
+  cudaError_t e = attn_grid(reinterpret_cast<const void*>(sparse_attn_prefill_kernel), items, &grid);
   if (e != cudaSuccess) return e;
   sparse_attn_prefill_kernel<<<grid, kAWarps * 32, kASmemBytes, st>>>(q, k, v, L_cap, q_pos, idx, count, B, n_q,
                                                                     Hq, Hkv, r, k_b, scale, out, lse);
@@ -488,12 +487,10 @@ cudaError_t launch_sparse_attn_decode(const __nv_bfloat16* q, const __nv_bfloat1
   // As many splits per unit as fill the resident warps once (at least one,
   // at most max_split), each a whole number of 16-slot groups.
   int grid = 0;
-  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), 1, units * max_split, &grid);
+  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), units * max_split, &grid);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
   int64_t n_split = (int64_t)sms * kAWarps / units;
   n_split = n_split < 1 ? 1 : (n_split > max_split ? max_split : n_split);
@@ -501,7 +498,7 @@ cudaError_t launch_sparse_attn_decode(const __nv_bfloat16* q, const __nv_bfloat1
   int split_len = (int)((max_tok + n_split - 1) / n_split);
   split_len = (split_len + kAGroup - 1) / kAGroup * kAGroup;
   n_split = (max_tok + split_len - 1) / split_len;
-  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), 1, units * n_split, &grid);
+  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), units * n_split, &grid);
   if (e != cudaSuccess) return e;
   sparse_attn_decode_kernel<<<grid, kAWarps * 32, kASmemBytes, st>>>(
       q, k, v, L_cap, cache_len, idx, count, B, n_q, Hq, Hkv, r, k_b, (int)n_split, split_len, scale, part_o, part_ml,

@@ -10,7 +10,6 @@ asks for) and streams.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from dataclasses import dataclass
 
@@ -28,7 +27,7 @@ EXPORTED = [
     "qsa_index_topk_workspace", "qsa_index_topk", "qsa_index_topk_fallback_rows", "qsa_sparse_attn_prefill",
     "qsa_sparse_attn_decode_workspace", "qsa_sparse_attn_decode", "qsa_sparse_attn_decode_noalloc",
     "qsa_sparse_attn_decode_multi_workspace", "qsa_sparse_attn_decode_multi",
-    "qsa_probe_l2_gather", "qsa_selftest_wait_timeout", "qsa_status_string",
+    "qsa_selftest_wait_timeout", "qsa_status_string",
     "qsa_read_device_error", "qsa_launch_count", "qsa_version",
 ]
 
@@ -59,7 +58,12 @@ class Config:
 
     @property
     def k_b(self) -> int:
-        return -(-self.k_tokens // self.r)
+        """Selected blocks per token, as the library computes it (qsa_num_selected_blocks)."""
+        c = self.c_struct()
+        k_b = int(load_library().qsa_num_selected_blocks(ctypes.byref(c)))
+        if k_b <= 0:
+            raise ValueError(f"invalid QSA configuration: {self}")
+        return k_b
 
     def c_struct(self) -> qsa_config:
         return qsa_config(self.r, self.n_idx_heads, self.head_dim, self.rope_dims, self.rope_base,
@@ -93,7 +97,6 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qsa_sparse_attn_decode_multi": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, I32, F, P, P, P, SZ,
                                                         P]),
         "qsa_sparse_attn_decode_noalloc": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, F, P, P, P]),
-        "qsa_probe_l2_gather": (ctypes.c_int, [P, SZ, ctypes.POINTER(ctypes.c_float), P]),
         "qsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "qsa_read_device_error": (ctypes.c_int, [P]),
         "qsa_selftest_wait_timeout": (ctypes.c_int, [I64, P]),
@@ -190,8 +193,7 @@ def qsa_sparse_attn_prefill(cfg: Config, q: torch.Tensor, k: torch.Tensor, v: to
     _i64(q_pos, "q_pos")
     B, n_q, Hq, d = q.shape
     Hkv, L_cap = k.shape[1], k.shape[2]
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
+    scale = 0.0 if scale is None else scale  # <= 0: the library's default 1/sqrt(head_dim)
     c = cfg.c_struct()
     _check("qsa_sparse_attn_prefill", load_library().qsa_sparse_attn_prefill(
         ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), L_cap, _ptr(q_pos), _ptr(idx), _ptr(count), B,
@@ -214,8 +216,7 @@ def qsa_sparse_attn_decode(cfg: Config, q: torch.Tensor, k_cache: torch.Tensor,
     _i64(cache_len, "cache_len")
     B, Hq, d = q.shape
     Hkv, L_cap = k_cache.shape[1], k_cache.shape[2]
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
+    scale = 0.0 if scale is None else scale  # <= 0: the library's default 1/sqrt(head_dim)
     c = cfg.c_struct()
     _check("qsa_sparse_attn_decode", load_library().qsa_sparse_attn_decode(
         ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), L_cap, _ptr(cache_len), _ptr(idx),
@@ -240,8 +241,7 @@ def qsa_sparse_attn_decode_multi(cfg: Config, q: torch.Tensor, k_cache: torch.Te
     _i64(cache_len, "cache_len")
     B, n_q, Hq, d = q.shape
     Hkv, L_cap = k_cache.shape[1], k_cache.shape[2]
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
+    scale = 0.0 if scale is None else scale  # <= 0: the library's default 1/sqrt(head_dim)
     c = cfg.c_struct()
     _check("qsa_sparse_attn_decode_multi", load_library().qsa_sparse_attn_decode_multi(
         ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), L_cap, _ptr(cache_len), _ptr(idx),
@@ -265,20 +265,11 @@ def qsa_sparse_attn_decode_noalloc(cfg: Config, q: torch.Tensor, k_cache: torch.
     _i64(cache_len, "cache_len")
     B, Hq, d = q.shape
     Hkv, L_cap = k_cache.shape[1], k_cache.shape[2]
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
+    scale = 0.0 if scale is None else scale  # <= 0: the library's default 1/sqrt(head_dim)
     c = cfg.c_struct()
     _check("qsa_sparse_attn_decode_noalloc", load_library().qsa_sparse_attn_decode_noalloc(
         ctypes.byref(c), _ptr(q), _ptr(k_cache), _ptr(v_cache), L_cap, _ptr(cache_len), _ptr(idx),
         _ptr(count), B, Hq, Hkv, scale, _ptr(out), _ptr(lse), _stream(stream)))
-
-
-def qsa_probe_l2_gather(buf: torch.Tensor, stream=None) -> float:
-    """GB/s of pseudo-random 256-byte row gathers from `buf` (a device tensor)."""
-    out = ctypes.c_float(0.0)
-    _check("qsa_probe_l2_gather", load_library().qsa_probe_l2_gather(
-        _ptr(buf), buf.numel() * buf.element_size(), ctypes.byref(out), _stream(stream)))
-    return float(out.value)
 
 
 def qsa_read_device_error(stream=None) -> int:

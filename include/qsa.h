@@ -22,9 +22,9 @@
  *     (`ws`, `ws_bytes`), whose required size the matching *_workspace() call
  *     returns.  Workspace pointers must be 256-byte aligned.
  *   - Every call is ordered on `stream` and returns without synchronising,
- *     except the three that read a value back to the host
- *     (qsa_index_topk_fallback_rows, qsa_probe_l2_gather, qsa_read_device_error),
- *     which synchronise `stream` first.
+ *     except the two that read a value back to the host
+ *     (qsa_index_topk_fallback_rows, qsa_read_device_error), which synchronise
+ *     `stream` first.
  *   - Arguments are checked on the host before any launch.  A bad argument
  *     returns QSA_ERR_INVALID_ARG and launches nothing; a shape outside what the
  *     kernels are built for returns QSA_ERR_UNSUPPORTED; a launch failure returns
@@ -164,6 +164,8 @@ qsa_status qsa_index_topk_fallback_rows(const qsa_config* cfg, int64_t B, int64_
  *   k, v   bf16 [B][Hkv][L_cap][head_dim]; every token of T_i must be < L_cap.
  *   q_pos  device int64 [B] as for qsa_index_topk (chunked prefill = q_pos > 0).
  *   idx, count  as written by qsa_index_topk.
+ *   scale  softmax scale; a value <= 0 selects 1 / sqrt(head_dim).  Not finite:
+ *          QSA_ERR_INVALID_ARG.  (The same holds for every attention call below.)
  *   out    bf16 [B][n_q][Hq][head_dim];  lse  fp32 [B][n_q][Hq] or NULL.
  * Softmax runs in fp32 with a running maximum; QK^T and PV accumulate in fp32.
  */
@@ -242,8 +244,14 @@ qsa_status qsa_sparse_attn_decode_multi(const qsa_config* cfg, const void* q, co
  *     call.  Its first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture on that device.
- *   Sharing: every call on a device uses the same array, and nothing in it has
- *     to start at zero (each call writes every partial it later reads).  Calls
+ *   Devices: the scratch array exists once per device, so the current device
+ *     must own `stream` and the tensors on every call; a stream or query tensor
+ *     of another device returns QSA_ERR_INVALID_ARG.
+ *   Sharing: every call on a device uses the same array, which keeps whatever
+ *     the last call left in it.  Nothing in it has to start at zero: each call
+ *     writes the maximum and sum of every split it combines, and the combine
+ *     skips the partial output of a split whose maximum is -inf (an empty
+ *     split), so stale values, even Inf or NaN, never reach a result.  Calls
  *     whose kernels can overlap on the GPU (different streams without ordering
  *     between them) race on the array and give wrong results; order them.
  */
@@ -253,17 +261,6 @@ qsa_status qsa_sparse_attn_decode_noalloc(const qsa_config* cfg, const void* q,
                                           const int32_t* idx, const int32_t* count, int64_t B,
                                           int32_t Hq, int32_t Hkv, float scale, void* out,
                                           float* lse, qsa_stream_t stream);
-
-/*
- * Measurement helper (not part of the method): the bandwidth at which the SMs
- * gather pseudo-random 256-byte rows from `buf` (`bytes` long, 256-byte
- * aligned, at least 1 MiB; contents are read, not modified, except its last
- * 256 bytes).  Sparse core attention gathers one 256-byte K row and one V row
- * per selected token, so with a buffer the size of one kv head's K/V (which
- * stays in L2) this is the bound of qsa_sparse_attn_prefill.  Synchronises
- * `stream`; writes GB/s to *gbs.  Allocates nothing.
- */
-qsa_status qsa_probe_l2_gather(void* buf, size_t bytes, float* gbs, qsa_stream_t stream);
 
 /* Human-readable name of a status. */
 const char* qsa_status_string(qsa_status s);

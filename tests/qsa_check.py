@@ -70,35 +70,56 @@ def check_selection_row(scores: np.ndarray, oracle_sel: np.ndarray, gpu_idx: np.
 
 
 def oracle_rows(wl: dict, rows, *, cfg, with_attention=True, q_pos0: int = 0) -> dict:
-    """Oracle prefill results for `rows` of sequence 0 of a workload dict."""
-    return O.prefill_rows(
-        bf16_to_np32(wl["q_idx"][0]), bf16_to_np(wl["k_idx"][0]), bf16_to_np32(wl["q"][0]),
-        bf16_to_np32(wl["k"][0]), bf16_to_np32(wl["v"][0]), rows, r=cfg.r, k_tokens=cfg.k_tokens,
-        q_pos0=q_pos0, rope_dims=cfg.rope_dims, rope_base=cfg.rope_base, rmsnorm=cfg.rmsnorm,
-        rms_eps=cfg.rms_eps, with_attention=with_attention)
+    """Oracle prefill results for `rows` of sequence 0 of a workload dict.  The
+    attention inputs ride along in res["attn"], so that rows whose selection is
+    an accepted near-tie swap can be re-attended on the GPU's own selection."""
+    q, k, v = bf16_to_np32(wl["q"][0]), bf16_to_np32(wl["k"][0]), bf16_to_np32(wl["v"][0])
+    res = O.prefill_rows(
+        bf16_to_np32(wl["q_idx"][0]), bf16_to_np(wl["k_idx"][0]), q, k, v, rows, r=cfg.r,
+        k_tokens=cfg.k_tokens, q_pos0=q_pos0, rope_dims=cfg.rope_dims, rope_base=cfg.rope_base,
+        rmsnorm=cfg.rmsnorm, rms_eps=cfg.rms_eps, with_attention=with_attention)
+    res["attn"] = (q, k, v)
+    return res
 
 
 def compare_prefill(res: dict, idx: np.ndarray, count: np.ndarray, out: np.ndarray | None,
-                    lse: np.ndarray | None, k_b: int, r: int, row_offset: int = 0) -> dict:
-    """Checks GPU idx/count (and out/lse on exactly-matching rows) against oracle rows.
+                    lse: np.ndarray | None, k_b: int, r: int, row_offset: int = 0, attn=None,
+                    scale: float | None = None) -> dict:
+    """Checks GPU idx/count and out/lse against oracle rows.
 
     idx/count/out/lse are indexed by query row (row j of the chunk); res["rows"]
-    lists which rows the oracle computed.  Returns counts of exact / margin rows.
+    lists which rows the oracle computed.  On a row whose selection matches the
+    oracle's, out/lse are compared with the oracle's own attention; on a row
+    accepted as a near-tie swap ("margin"), with the oracle's attention over the
+    token set of the GPU's selection (its blocks plus the row's tail), computed
+    from `attn` = (q [n_q, Hq, d], k [Hkv, L, d], v) or res["attn"].  Returns
+    counts of exact / margin rows and the largest errors.
     """
     stats = {"exact": 0, "margin": 0, "max_out_err": 0.0, "max_lse_err": 0.0}
+    if attn is None:
+        attn = res.get("attn")
     for n, j in enumerate(res["rows"]):
         i = int(res["pos"][n])
         c = O.visible_blocks(i, r)
         kind = check_selection_row(res["scores"][n], res["sel"][n], idx[j], int(count[j]), c, k_b)
         stats[kind] += 1
-        if out is not None and kind == "exact" and res["out"] is not None:
-            err = float(np.abs(out[j] - res["out"][n]).max())
-            assert err <= OUT_ATOL, f"row {j}: output error {err}"
-            stats["max_out_err"] = max(stats["max_out_err"], err)
-            if lse is not None:
-                e2 = float(np.abs(lse[j] - res["lse"][n]).max())
-                assert e2 <= LSE_ATOL, f"row {j}: lse error {e2}"
-                stats["max_lse_err"] = max(stats["max_lse_err"], e2)
+        if out is None or res["out"] is None:
+            continue
+        if kind == "exact":
+            want_o, want_l = res["out"][n], res["lse"][n]
+        else:
+            assert attn is not None, f"row {j}: near-tie row without attention inputs to check its output"
+            q, k, v = attn
+            sc = default_scale(q.shape[-1]) if scale is None else scale
+            toks = O.token_set(i, idx[j][:int(count[j])].astype(np.int64), r)
+            want_o, want_l = O.attend(np.asarray(q[res["rows"][n]], np.float64), k, v, toks, sc)
+        err = float(np.abs(out[j] - want_o).max())
+        assert err <= OUT_ATOL, f"row {j} ({kind}): output error {err}"
+        stats["max_out_err"] = max(stats["max_out_err"], err)
+        if lse is not None:
+            e2 = float(np.abs(lse[j] - want_l).max())
+            assert e2 <= LSE_ATOL, f"row {j} ({kind}): lse error {e2}"
+            stats["max_lse_err"] = max(stats["max_lse_err"], e2)
     return stats
 
 

@@ -263,11 +263,11 @@ def test_batched_prefill_sequences_at_different_offsets():
     rows = [0, 1, 250, 498, 499]
     exact = 0
     for b, o in enumerate(offs):
-        res = O.prefill_rows(QC.bf16_to_np32(q_idx[b]), QC.bf16_to_np(wl["k_idx"][b]), QC.bf16_to_np32(q[b]),
-                             QC.bf16_to_np32(wl["k"][b]), QC.bf16_to_np32(wl["v"][b]), rows, r=cfg.r,
+        qb, kb, vb = QC.bf16_to_np32(q[b]), QC.bf16_to_np32(wl["k"][b]), QC.bf16_to_np32(wl["v"][b])
+        res = O.prefill_rows(QC.bf16_to_np32(q_idx[b]), QC.bf16_to_np(wl["k_idx"][b]), qb, kb, vb, rows, r=cfg.r,
                              k_tokens=cfg.k_tokens, q_pos0=o, rope_dims=cfg.rope_dims, rope_base=cfg.rope_base)
         st = QC.compare_prefill(res, idx[b].cpu().numpy(), cnt[b].cpu().numpy(), out[b].float().cpu().numpy(),
-                                lse[b].cpu().numpy(), cfg.k_b, cfg.r)
+                                lse[b].cpu().numpy(), cfg.k_b, cfg.r, attn=(qb, kb, vb))
         exact += st["exact"]
     assert exact >= 3 * len(rows) - 1
 
@@ -328,8 +328,13 @@ def check_decode_seq(cfg, wl, bb, idx, cnt, out, lse):
     kind = QC.check_selection_row(res["scores"][0], res["sel"][0], idx[bb], int(cnt[bb]),
                                   O.visible_blocks(L - 1, cfg.r), cfg.k_b)
     if kind == "exact":
-        assert np.abs(out[bb] - res["out"][0]).max() <= QC.OUT_ATOL
-        assert np.abs(lse[bb] - res["lse"][0]).max() <= QC.LSE_ATOL
+        want_o, want_l = res["out"][0], res["lse"][0]
+    else:  # a near-tie swap: the oracle's attention over the GPU's own selection
+        toks = O.token_set(L - 1, idx[bb][:int(cnt[bb])].astype(np.int64), cfg.r)
+        want_o, want_l = O.attend(QC.bf16_to_np(wl["q"][bb, 0]), QC.bf16_to_np32(wl["k"][bb]),
+                                  QC.bf16_to_np32(wl["v"][bb]), toks, QC.default_scale(128))
+    assert np.abs(out[bb] - want_o).max() <= QC.OUT_ATOL
+    assert np.abs(lse[bb] - want_l).max() <= QC.LSE_ATOL
     return kind
 
 
@@ -352,6 +357,27 @@ def test_decode_ragged_cache_lengths():
     idx, cnt, out, lse = run_decode(cfg, wl)
     for bb in range(4):
         check_decode_seq(cfg, wl, bb, idx, cnt, out, lse)
+
+
+def test_decode_ignores_nonfinite_workspace_contents():
+    """The decode workspace holds whatever its last user left (here: NaN in every
+    byte).  Short and ragged caches leave most splits empty; their partial
+    outputs are never written and must not enter the combine."""
+    spec = DecodeSpec("d", batch=3, ctx=9000, k_tokens=2048, seed=23)
+    wl = make_decode(spec, DEV)
+    wl["cache_lens"] = torch.tensor([3, 17, 9001], dtype=torch.int64, device=DEV)
+    cfg = cfg_for(spec)
+    B = 3
+    dec = qsa.QsaDecode(cfg, B, wl["n_blocks"], 16, 2)
+    dec.ws_attn.fill_(0xFF)  # 0xFFFFFFFF is a NaN in every fp32 slot
+    out = dec(wl["q_idx"], wl["q"][:, 0].contiguous(), wl["kbar"], wl["k"], wl["v"], wl["cache_lens"])
+    torch.cuda.synchronize()
+    assert qsa.qsa_read_device_error() == 0
+    o, lse = out.float().cpu().numpy(), dec.lse.cpu().numpy()
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    idx, cnt = dec.idx.view(B, -1).cpu().numpy(), dec.count.view(B).cpu().numpy()
+    for bb in range(B):
+        check_decode_seq(cfg, wl, bb, idx, cnt, o, lse)
 
 
 @pytest.mark.slow
@@ -388,12 +414,12 @@ def check_decode_multi_seq(cfg, wl, bb, idx, cnt, out, lse):
     """Rows j of sequence bb are tokens L - next_n + j; the oracle scores them
     against the given compressed-key cache like prefill rows at those positions."""
     L, nn = int(wl["cache_lens"][bb]), wl["q"].shape[1]
-    res = O.prefill_rows(QC.bf16_to_np32(wl["q_idx"][bb]), None, QC.bf16_to_np32(wl["q"][bb]),
-                         QC.bf16_to_np32(wl["k"][bb]), QC.bf16_to_np32(wl["v"][bb]), range(nn), r=cfg.r,
+    qb, kb, vb = QC.bf16_to_np32(wl["q"][bb]), QC.bf16_to_np32(wl["k"][bb]), QC.bf16_to_np32(wl["v"][bb])
+    res = O.prefill_rows(QC.bf16_to_np32(wl["q_idx"][bb]), None, qb, kb, vb, range(nn), r=cfg.r,
                          k_tokens=cfg.k_tokens, q_pos0=L - nn, rope_dims=cfg.rope_dims, rope_base=cfg.rope_base,
                          kbar=QC.bf16_to_np(wl["kbar"][bb]))
     return QC.compare_prefill(res, idx[bb].cpu().numpy(), cnt[bb].cpu().numpy(), out[bb].float().cpu().numpy(),
-                              lse[bb].cpu().numpy(), cfg.k_b, cfg.r)
+                              lse[bb].cpu().numpy(), cfg.k_b, cfg.r, attn=(qb, kb, vb))
 
 
 @pytest.mark.parametrize("next_n,ctx", [(2, 3001), (3, 5003), (4, 4096), (4, 700)])
@@ -484,27 +510,78 @@ def test_million_token_prefill_sampled_rows():
     rows = QC.sample_rows(n, cfg.k_b, cfg.r, needle_rows, 16, seed=spec.seed)
     exact = 0
     for i in rows:
-        res = O.prefill_rows(QC.bf16_to_np32(wl["q_idx"][0, i:i + 1]), None, QC.bf16_to_np32(wl["q"][0, i:i + 1]),
+        qi = QC.bf16_to_np32(wl["q"][0, i:i + 1])
+        res = O.prefill_rows(QC.bf16_to_np32(wl["q_idx"][0, i:i + 1]), None, qi,
                              k, v, [0], r=cfg.r, k_tokens=cfg.k_tokens, q_pos0=i, rope_dims=cfg.rope_dims,
                              rope_base=cfg.rope_base, kbar=kb_o)
         st = QC.compare_prefill(res, idx[0, i:i + 1].cpu().numpy(), cnt[0, i:i + 1].cpu().numpy(),
-                                out[0, i:i + 1].float().cpu().numpy(), lse[0, i:i + 1].cpu().numpy(), cfg.k_b, cfg.r)
+                                out[0, i:i + 1].float().cpu().numpy(), lse[0, i:i + 1].cpu().numpy(), cfg.k_b, cfg.r,
+                                attn=(qi, k, v))
         exact += st["exact"]
     assert exact >= 0.9 * len(rows), (exact, len(rows))
 
 
 # ----------------------------------------------------------------------------- full-size prefill, sampled rows
 
-@pytest.mark.slow
-@pytest.mark.parametrize("name", ["needle_prefill_32k", "drift_prefill_128k"])
-def test_large_prefill_sampled_rows(name):
-    spec = WORKLOADS[name]
+@pytest.fixture(scope="module")
+def prefill_128k():
+    """One GPU prefill of drift_prefill_128k in the bench's launch configuration,
+    shared by the tests below."""
+    spec = WORKLOADS["drift_prefill_128k"]
     wl = make_prefill(spec, DEV)
     cfg = cfg_for(spec)
-    gpu = run_prefill(cfg, wl)
+    return spec, cfg, wl, run_prefill(cfg, wl)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["needle_prefill_32k", "drift_prefill_128k"])
+def test_large_prefill_sampled_rows(name, request):
+    if name == "drift_prefill_128k":
+        spec, cfg, wl, gpu = request.getfixturevalue("prefill_128k")
+    else:
+        spec = WORKLOADS[name]
+        wl = make_prefill(spec, DEV)
+        cfg = cfg_for(spec)
+        gpu = run_prefill(cfg, wl)
     needle_rows = [i for (_, i, _) in wl["needles"]][:16]
     rows = QC.sample_rows(spec.n, cfg.k_b, cfg.r, needle_rows, 24, seed=spec.seed)
     res = QC.oracle_rows(wl, rows, cfg=cfg)
     st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0],
                             cfg.k_b, cfg.r)
     assert st["exact"] >= 0.9 * len(rows), st
+
+
+# The prefill indexer works on tiles of 48 consecutive query rows and the host
+# launches it over ranges of at most 1024 tiles, the last range first.  At
+# n = 131072 (2731 tiles) the ranges are tiles 1707-2730, 683-1706 and 0-682.
+INDEX_TILE_ROWS = 48
+INDEX_TILES_PER_LAUNCH = 1024
+
+
+def seam_tiles(n: int) -> list[int]:
+    """First tile, the tiles on each side of every launch seam, the tile where
+    rows start to choose (c_i crosses k_B = 512 at row 2047) and the last tile."""
+    n_tiles = -(-n // INDEX_TILE_ROWS)
+    tiles = {0, 2047 // INDEX_TILE_ROWS, n_tiles - 1}
+    for t_end in range(n_tiles, 0, -INDEX_TILES_PER_LAUNCH):
+        t_begin = max(0, t_end - INDEX_TILES_PER_LAUNCH)
+        if t_begin > 0:
+            tiles |= {t_begin - 1, t_begin}
+    return sorted(tiles)
+
+
+@pytest.mark.slow
+def test_prefill_128k_whole_tiles_at_launch_seams(prefill_128k):
+    """Every row of whole indexer tiles at 128K: the first and last tiles, the
+    tile where selection starts, and the tiles on both sides of each launch
+    seam; selection, output and LSE of every row against the oracle."""
+    spec, cfg, wl, gpu = prefill_128k
+    tiles = seam_tiles(spec.n)
+    assert {682, 683, 1706, 1707, 0, 2730} <= set(tiles)
+    rows = [j for t in tiles for j in range(t * INDEX_TILE_ROWS, min(spec.n, (t + 1) * INDEX_TILE_ROWS))]
+    assert 32784 in rows and 81936 in rows and 131071 in rows
+    res = QC.oracle_rows(wl, rows, cfg=cfg)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0],
+                            cfg.k_b, cfg.r)
+    assert st["exact"] + st["margin"] == len(rows)
+    assert st["exact"] >= 0.97 * len(rows), st

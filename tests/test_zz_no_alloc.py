@@ -7,6 +7,8 @@ point, including on back-to-back calls, where the second call finds the first
 call's partials still in the shared array.  This file is named to be collected
 last, so a failing run that stops at the first failure has run every other test.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -77,3 +79,37 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
     with pytest.raises(qsa.QsaError) as ei:
         qsa.qsa_sparse_attn_decode_noalloc(cfg, q, kc, kc, cl, idx, cnt, out)
     assert ei.value.status == 3  # QSA_ERR_WORKSPACE
+
+
+def test_noalloc_ignores_stale_nonfinite_partials():
+    """The shared array keeps what the last call left in it.  A first call whose
+    V holds Inf leaves non-finite partials behind; the next call, a ragged batch
+    with short caches (so that many of its splits are empty), must still match
+    the regular entry point and be finite."""
+    cfg, wl, idx, cnt = _decode_case(33, 8, 40000)
+    wl["v"][:, :, :4096] = float("inf")
+    q = wl["q"][:, 0].contiguous()
+    out = torch.empty((8, 16, 128), dtype=torch.bfloat16, device=DEV)
+    qsa.qsa_sparse_attn_decode_noalloc(cfg, q, wl["k"], wl["v"], wl["cache_lens"], idx, cnt, out)
+    torch.cuda.synchronize()
+    assert not torch.isfinite(out.float()).all()  # the poison reached the partials
+    cfg2, wl2, idx2, cnt2 = _decode_case(34, 5, 9000, cache_lens=[3, 17, 9001, 40, 2051])
+    ref, ref_lse, out2, lse2 = _both(cfg2, wl2, idx2, cnt2)
+    assert np.isfinite(out2).all() and np.isfinite(lse2).all()
+    assert np.abs(out2 - ref).max() <= QC.OUT_ATOL
+    assert np.abs(lse2 - ref_lse).max() <= QC.LSE_ATOL
+
+
+def test_noalloc_rejects_a_stream_of_another_device():
+    """The scratch array is per device: a tensor that is not device memory of the
+    current device is refused before any launch."""
+    cfg = qsa.Config()
+    q = torch.zeros((2, 16, 128), dtype=torch.bfloat16)  # host memory
+    lib = qsa.load_library()
+    c = cfg.c_struct()
+    fake = torch.zeros(16, dtype=torch.int64, device=DEV)
+    st = lib.qsa_sparse_attn_decode_noalloc(ctypes.byref(c), q.data_ptr(), fake.data_ptr(), fake.data_ptr(), 8,
+                                            fake.data_ptr(), fake.data_ptr(), fake.data_ptr(), 2, 16, 2, 0.0,
+                                            fake.data_ptr(), None, torch.cuda.current_stream().cuda_stream)
+    assert st == 1  # QSA_ERR_INVALID_ARG
+    assert qsa.qsa_read_device_error() == 0
