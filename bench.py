@@ -217,6 +217,24 @@ def chunked_prefill_measure(qsa, cfg, pspec, wl, pre, chunk: int, steps: int, wa
     return {"chunk_tokens": chunk, "prefix_tokens": lo, "ms_per_chunk": ms, "tokens_per_s": chunk / (ms * 1e-3)}
 
 
+def attention_kernels_measure(qsa, cfg, wl, pre, steps: int, warmup: int, flush) -> dict:
+    """Prefill attention alone, each kernel of the library on the same inputs
+    and selection (the last prefill's): the tcgen05 kernel (TMA-staged blocks,
+    TMEM accumulators) and the mma.sync one.  Median of CUDA-event timings, L2
+    flushed between runs."""
+    res = {}
+    for impl in ("tcgen05", "mma_sync"):
+        def step():
+            qsa.qsa_sparse_attn_prefill(cfg, wl["q"], wl["k"], wl["v"], pre.q_pos, pre.idx, pre.count,
+                                        pre.out, pre.lse, impl=impl)
+        try:
+            res[impl] = {"ms": _median_step_ms(step, steps, warmup, flush)}
+        except qsa.QsaError as ex:
+            res[impl] = {"unavailable": str(ex)}
+    assert qsa.qsa_read_device_error() == 0
+    return res
+
+
 def dense_decode_measure(qsa, dspec, dwl, dq, steps: int, warmup: int, dev, flush, hbm_gbs: float,
                          qsa_decode_us: float) -> dict:
     """Dense GQA decode at the decode step's shape, for the pages' form of
@@ -601,6 +619,13 @@ def main():
     if decode_multi is not None:
         line["decode_multi"] = decode_multi
     if not args.no_extras:
+        kern = attention_kernels_measure(qsa, cfg, wl, pre, args.steps, args.warmup, flush)
+        for impl, v in kern.items():
+            if "ms" in v:
+                v["tflops"] = pw["attn_flops"] / (v["ms"] * 1e-3) / 1e12
+                v["frac_of_burst"] = v["tflops"] / pk["bf16_tflops"]
+                v["gathered_tb_s"] = pw["attn_gather_bytes"] / (v["ms"] * 1e-3) / 1e12
+        line["rooflines"]["attn_prefill"]["kernels"] = kern
         chunk = min(16384, pspec.n)
         line["chunked_prefill"] = chunked_prefill_measure(qsa, cfg, pspec, wl, pre, chunk, args.steps, args.warmup,
                                                           dev, flush)

@@ -10,6 +10,7 @@
 #include "topk_select.cu"
 #include "index_fused.cu"
 #include "sparse_attn.cu"
+#include "sparse_attn_tc.cu"
 
 namespace qsa {
 namespace {
@@ -195,23 +196,43 @@ qsa_status qsa_index_topk_fallback_rows(const qsa_config* cfg, int64_t B, int64_
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
+qsa_status qsa_sparse_attn_prefill_impl(const qsa_config* cfg, const void* q, const void* k,
+                                        const void* v, int64_t L_cap, const int64_t* q_pos,
+                                        const int32_t* idx, const int32_t* count, int64_t B,
+                                        int64_t n_q, int32_t Hq, int32_t Hkv, float scale, void* out,
+                                        float* lse, qsa_attn_impl impl, qsa_stream_t stream) {
+  qsa_status s = check_config(cfg);
+  if (s != QSA_OK) return s;
+  if (B < 0 || n_q < 0 || L_cap < 0 || Hq < 1 || Hkv < 1 || !std::isfinite(scale)) return QSA_ERR_INVALID_ARG;
+  if (impl != QSA_ATTN_AUTO && impl != QSA_ATTN_TCGEN05 && impl != QSA_ATTN_MMA_SYNC) return QSA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return QSA_ERR_UNSUPPORTED;
+  const bool tc_ok = tc_attention_supported(Hq, Hkv, cfg->r);
+  if (impl == QSA_ATTN_TCGEN05 && !tc_ok) return QSA_ERR_UNSUPPORTED;
+  if (B == 0 || n_q == 0) return QSA_OK;
+  if (!q || !k || !v || !q_pos || !idx || !count || !out || L_cap < 1) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return QSA_ERR_INVALID_ARG;
+  const auto* qb = static_cast<const __nv_bfloat16*>(q);
+  const auto* kb = static_cast<const __nv_bfloat16*>(k);
+  const auto* vb = static_cast<const __nv_bfloat16*>(v);
+  auto* ob = static_cast<__nv_bfloat16*>(out);
+  const float sc = softmax_scale(cfg, scale);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // AUTO takes the mma.sync kernel: on B300 it gathers at about 11.5 TB/s
+  // against 3.5 TB/s for the TMA-fed tcgen05 kernel at every supported r.
+  if (impl == QSA_ATTN_TCGEN05)
+    return from_cuda(launch_sparse_attn_tc(qb, kb, vb, L_cap, q_pos, idx, count, B, n_q, Hq, Hkv, cfg->r,
+                                           k_blocks(cfg), sc, ob, lse, st));
+  return from_cuda(launch_sparse_attn_prefill(qb, kb, vb, L_cap, q_pos, idx, count, B, n_q, Hq, Hkv, cfg->r,
+                                              k_blocks(cfg), sc, ob, lse, st));
+}
+
 qsa_status qsa_sparse_attn_prefill(const qsa_config* cfg, const void* q, const void* k,
                                    const void* v, int64_t L_cap, const int64_t* q_pos,
                                    const int32_t* idx, const int32_t* count, int64_t B,
                                    int64_t n_q, int32_t Hq, int32_t Hkv, float scale, void* out,
                                    float* lse, qsa_stream_t stream) {
-  qsa_status s = check_config(cfg);
-  if (s != QSA_OK) return s;
-  if (B < 0 || n_q < 0 || L_cap < 0 || Hq < 1 || Hkv < 1 || !std::isfinite(scale)) return QSA_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0) return QSA_ERR_UNSUPPORTED;
-  if (B == 0 || n_q == 0) return QSA_OK;
-  if (!q || !k || !v || !q_pos || !idx || !count || !out || L_cap < 1) return QSA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return QSA_ERR_INVALID_ARG;
-  return from_cuda(launch_sparse_attn_prefill(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-      static_cast<const __nv_bfloat16*>(v), L_cap, q_pos, idx, count, B, n_q, Hq, Hkv, cfg->r,
-      k_blocks(cfg), softmax_scale(cfg, scale), static_cast<__nv_bfloat16*>(out), lse,
-      reinterpret_cast<cudaStream_t>(stream)));
+  return qsa_sparse_attn_prefill_impl(cfg, q, k, v, L_cap, q_pos, idx, count, B, n_q, Hq, Hkv, scale, out, lse,
+                                      QSA_ATTN_AUTO, stream);
 }
 
 size_t qsa_sparse_attn_decode_workspace(const qsa_config* cfg, int64_t B, int32_t Hq, int32_t Hkv) {

@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED",
 EXPORTED = [
     "qsa_default_config", "qsa_num_selected_blocks", "qsa_compress_keys",
     "qsa_index_topk_workspace", "qsa_index_topk", "qsa_index_topk_fallback_rows", "qsa_sparse_attn_prefill",
+    "qsa_sparse_attn_prefill_impl",
     "qsa_sparse_attn_decode_workspace", "qsa_sparse_attn_decode", "qsa_sparse_attn_decode_noalloc",
     "qsa_sparse_attn_decode_multi_workspace", "qsa_sparse_attn_decode_multi",
     "qsa_selftest_wait_timeout", "qsa_status_string",
@@ -91,6 +92,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qsa_index_topk": (ctypes.c_int, [C, P, P, I64, P, I64, I64, I64, P, P, P, SZ, P]),
         "qsa_index_topk_fallback_rows": (ctypes.c_int, [C, I64, I64, I64, P, SZ, ctypes.POINTER(I64), P]),
         "qsa_sparse_attn_prefill": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I64, I32, I32, F, P, P, P]),
+        "qsa_sparse_attn_prefill_impl": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I64, I32, I32, F, P, P,
+                                                        ctypes.c_int, P]),
         "qsa_sparse_attn_decode_workspace": (SZ, [C, I64, I32, I32]),
         "qsa_sparse_attn_decode": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I32, I32, F, P, P, P, SZ, P]),
         "qsa_sparse_attn_decode_multi_workspace": (SZ, [C, I64, I32, I32, I32]),
@@ -183,11 +186,17 @@ def qsa_index_topk_fallback_rows(cfg: Config, B: int, n_q: int, n_blocks_max: in
     return int(rows.value)
 
 
+# Kernel choice of qsa_sparse_attn_prefill_impl (qsa_attn_impl in include/qsa.h).
+QSA_ATTN_AUTO, QSA_ATTN_TCGEN05, QSA_ATTN_MMA_SYNC = 0, 1, 2
+ATTN_IMPLS = {"auto": QSA_ATTN_AUTO, "tcgen05": QSA_ATTN_TCGEN05, "mma_sync": QSA_ATTN_MMA_SYNC}
+
+
 def qsa_sparse_attn_prefill(cfg: Config, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                             q_pos: torch.Tensor, idx: torch.Tensor, count: torch.Tensor,
                             out: torch.Tensor, lse: torch.Tensor | None = None,
-                            scale: float | None = None, stream=None) -> None:
-    """q [B, n_q, Hq, d]; k, v [B, Hkv, L_cap, d]; out like q; lse [B, n_q, Hq] fp32 or None."""
+                            scale: float | None = None, stream=None, impl: str = "auto") -> None:
+    """q [B, n_q, Hq, d]; k, v [B, Hkv, L_cap, d]; out like q; lse [B, n_q, Hq] fp32 or None.
+    impl: "auto" (the library's choice), "tcgen05" or "mma_sync"."""
     for t, nm in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
         _bf16(t, nm)
     _i64(q_pos, "q_pos")
@@ -195,9 +204,9 @@ def qsa_sparse_attn_prefill(cfg: Config, q: torch.Tensor, k: torch.Tensor, v: to
     Hkv, L_cap = k.shape[1], k.shape[2]
     scale = 0.0 if scale is None else scale  # <= 0: the library's default 1/sqrt(head_dim)
     c = cfg.c_struct()
-    _check("qsa_sparse_attn_prefill", load_library().qsa_sparse_attn_prefill(
+    _check("qsa_sparse_attn_prefill_impl", load_library().qsa_sparse_attn_prefill_impl(
         ctypes.byref(c), _ptr(q), _ptr(k), _ptr(v), L_cap, _ptr(q_pos), _ptr(idx), _ptr(count), B,
-        n_q, Hq, Hkv, scale, _ptr(out), _ptr(lse), _stream(stream)))
+        n_q, Hq, Hkv, scale, _ptr(out), _ptr(lse), ATTN_IMPLS[impl], _stream(stream)))
 
 
 def qsa_sparse_attn_decode_workspace(cfg: Config, B: int, Hq: int, Hkv: int) -> int:

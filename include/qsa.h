@@ -175,6 +175,27 @@ qsa_status qsa_sparse_attn_prefill(const qsa_config* cfg, const void* q, const v
                                    int64_t n_q, int32_t Hq, int32_t Hkv, float scale, void* out,
                                    float* lse, qsa_stream_t stream);
 
+/* Kernel choice for qsa_sparse_attn_prefill_impl. */
+typedef enum {
+  QSA_ATTN_AUTO = 0,     /* the faster kernel for the shape (what qsa_sparse_attn_prefill does):
+                            the mma.sync kernel, measured faster on B300 for every r */
+  QSA_ATTN_TCGEN05 = 1,  /* TMA-staged micro-blocks, tcgen05 MMAs with TMEM accumulators; needs
+                            Hq = 8 Hkv and r in {4, 8, 16}, else QSA_ERR_UNSUPPORTED */
+  QSA_ATTN_MMA_SYNC = 2  /* per-warp cp.async gathers and m16n8k16 MMAs; any Hq % Hkv == 0, any r */
+} qsa_attn_impl;
+
+/*
+ * qsa_sparse_attn_prefill with an explicit kernel: the same arguments, results
+ * and errors, plus `impl` (QSA_ERR_INVALID_ARG for a value outside the enum).
+ * Both kernels compute the same function; they differ in rounding order only
+ * (fp32 accumulation in both, P rounded to bf16 before the PV product in both).
+ */
+qsa_status qsa_sparse_attn_prefill_impl(const qsa_config* cfg, const void* q, const void* k,
+                                        const void* v, int64_t L_cap, const int64_t* q_pos,
+                                        const int32_t* idx, const int32_t* count, int64_t B,
+                                        int64_t n_q, int32_t Hq, int32_t Hkv, float scale, void* out,
+                                        float* lse, qsa_attn_impl impl, qsa_stream_t stream);
+
 /* Workspace for qsa_sparse_attn_decode with the same (cfg, B, Hq, Hkv). */
 size_t qsa_sparse_attn_decode_workspace(const qsa_config* cfg, int64_t B, int32_t Hq,
                                         int32_t Hkv);

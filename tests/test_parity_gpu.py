@@ -26,8 +26,9 @@ def cfg_for(spec, **kw) -> qsa.Config:
     return qsa.Config(**base)
 
 
-def run_prefill(cfg: qsa.Config, wl: dict, q_pos0: int = 0, rows: slice | None = None):
-    """Full GPU prefill of sequence batch `wl` through the binding; returns numpy views."""
+def run_prefill(cfg: qsa.Config, wl: dict, q_pos0: int = 0, rows: slice | None = None, impl: str = "auto"):
+    """Full GPU prefill of sequence batch `wl` through the binding; returns numpy views.
+    impl picks the attention kernel ("auto", "tcgen05" or "mma_sync")."""
     q_idx, k_idx, q, k, v = wl["q_idx"], wl["k_idx"], wl["q"], wl["k"], wl["v"]
     if rows is not None:  # chunk of query rows at positions q_pos0 + j
         q_idx, q = q_idx[:, rows].contiguous(), q[:, rows].contiguous()
@@ -44,7 +45,7 @@ def run_prefill(cfg: qsa.Config, wl: dict, q_pos0: int = 0, rows: slice | None =
     fallback_rows = qsa.qsa_index_topk_fallback_rows(cfg, B, n_q, nb, ws)
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=DEV)
-    qsa.qsa_sparse_attn_prefill(cfg, q, k, v, q_pos, idx, cnt, out, lse)
+    qsa.qsa_sparse_attn_prefill(cfg, q, k, v, q_pos, idx, cnt, out, lse, impl=impl)
     torch.cuda.synchronize()
     assert qsa.qsa_read_device_error() == 0
     return {"kbar": kbar, "idx": idx.cpu().numpy(), "count": cnt.cpu().numpy(),
@@ -107,8 +108,9 @@ def test_tiny_prefill_selection_and_output_all_rows(tiny):
     assert st["margin"] <= spec.n // 100, st
 
 
-def test_tiny_attention_on_oracle_selection(tiny):
-    """The attention kernel alone, fed the oracle's own selection, on every row."""
+@pytest.mark.parametrize("impl", ["tcgen05", "mma_sync"])
+def test_tiny_attention_on_oracle_selection(tiny, impl):
+    """Each attention kernel alone, fed the oracle's own selection, on every row."""
     spec, cfg, wl, gpu, res = tiny
     n, k_b = spec.n, cfg.k_b
     idx = np.full((1, n, k_b), -1, dtype=np.int32)
@@ -121,7 +123,9 @@ def test_tiny_attention_on_oracle_selection(tiny):
     out = torch.empty_like(wl["q"])
     lse = torch.empty(wl["q"].shape[:3], dtype=torch.float32, device=DEV)
     qsa.qsa_sparse_attn_prefill(cfg, wl["q"], wl["k"], wl["v"], q_pos, torch.from_numpy(idx).to(DEV),
-                                torch.from_numpy(cnt).to(DEV), out, lse)
+                                torch.from_numpy(cnt).to(DEV), out, lse, impl=impl)
+    torch.cuda.synchronize()
+    assert qsa.qsa_read_device_error() == 0
     o = out.float().cpu().numpy()[0]
     assert np.abs(o - res["out"]).max() <= QC.OUT_ATOL
     assert np.abs(lse.cpu().numpy()[0] - res["lse"]).max() <= QC.LSE_ATOL
@@ -142,6 +146,7 @@ def small_case(n, k_tokens, r=4, hq=16, hkv=2, seed=3, rope_dims=64):
     return spec, make_prefill(spec, DEV)
 
 
+@pytest.mark.parametrize("impl", ["auto", "tcgen05"])
 @pytest.mark.parametrize("n,k_tokens,r,hq,hkv", [
     (1, 64, 4, 16, 2),       # one token, no complete block: tail only
     (3, 64, 4, 16, 2),       # n < r
@@ -151,16 +156,53 @@ def small_case(n, k_tokens, r=4, hq=16, hkv=2, seed=3, rope_dims=64):
     (300, 64, 4, 12, 4),     # group size 3: padded head chunk
     (401, 40, 2, 16, 2),     # r = 2, k_B = 20
     (777, 128, 8, 16, 2),    # r = 8
-    (515, 48, 16, 16, 1),    # r = 16, one kv head
+    (515, 48, 16, 16, 1),    # r = 16, one kv head, group size 16
+    (515, 48, 16, 8, 1),     # r = 16, one kv head, group size 8
+    (1999, 300, 4, 16, 2),   # k_B = 75: a last stage of 11 slots (odd, padded to a whole K-step)
 ])
-def test_edge_shapes_match_oracle(n, k_tokens, r, hq, hkv):
+def test_edge_shapes_match_oracle(n, k_tokens, r, hq, hkv, impl):
+    """Every shape through "auto" (the mma.sync kernel), and through the tcgen05
+    kernel where it applies (8 query heads per kv head, r in {4, 8, 16})."""
+    if impl == "tcgen05" and not (hq == 8 * hkv and r in (4, 8, 16)):
+        pytest.skip("shape outside the tcgen05 kernel (its refusal is tested separately)")
     spec, wl = small_case(n, k_tokens, r, hq, hkv)
     cfg = cfg_for(spec)
-    gpu = run_prefill(cfg, wl)
+    gpu = run_prefill(cfg, wl, impl=impl)
     res = QC.oracle_rows(wl, range(n), cfg=cfg)
     st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0],
                             cfg.k_b, cfg.r)
     assert st["exact"] >= 0.98 * n
+
+
+def test_tcgen05_kernel_refuses_unsupported_shapes():
+    """The tcgen05 kernel serves 8 query heads per kv head and r in {4, 8, 16};
+    asked for anything else it returns QSA_ERR_UNSUPPORTED and launches nothing."""
+    for (hq, hkv, r) in [(16, 1, 4), (12, 4, 4), (16, 2, 2)]:
+        spec, wl = small_case(64, 64, r, hq, hkv)
+        cfg = cfg_for(spec)
+        q_pos = torch.zeros((1,), dtype=torch.int64, device=DEV)
+        idx = torch.zeros((1, 64, cfg.k_b), dtype=torch.int32, device=DEV)
+        cnt = torch.zeros((1, 64), dtype=torch.int32, device=DEV)
+        out = torch.empty_like(wl["q"])
+        launches = qsa.qsa_launch_count()
+        with pytest.raises(qsa.QsaError) as ei:
+            qsa.qsa_sparse_attn_prefill(cfg, wl["q"], wl["k"], wl["v"], q_pos, idx, cnt, out, impl="tcgen05")
+        assert ei.value.status == 2
+        assert qsa.qsa_launch_count() == launches
+
+
+def test_tcgen05_and_mma_sync_kernels_agree_at_32k():
+    """The two attention kernels on the needle workload's own GPU selection: both
+    within the output tolerance of each other on every row (they differ in
+    rounding order only)."""
+    spec = WORKLOADS["needle_prefill_32k"]
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    a = run_prefill(cfg, wl, impl="tcgen05")
+    b = run_prefill(cfg, wl, impl="mma_sync")
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    assert np.abs(a["out"] - b["out"]).max() <= QC.OUT_ATOL
+    assert np.abs(a["lse"] - b["lse"]).max() <= QC.LSE_ATOL
 
 
 def test_dense_limit_equals_torch_sdpa():
