@@ -235,6 +235,55 @@ def attention_kernels_measure(qsa, cfg, wl, pre, steps: int, warmup: int, flush)
     return res
 
 
+def index_sweep_measure(qsa, pk: dict, steps: int, warmup: int, dev, flush, with_1m_r2: bool = False) -> list:
+    """qsa_index_topk alone (query rotation, scores, top-k_B) at micro-block
+    sizes r in {2, 4, 8, 16} over the 32K, 128K and 1M prefill workloads' indexer
+    inputs (K = 2048, 4 indexer heads), the form of the pages' indexer-latency
+    panels.  Each line: median ms over the timed calls (L2 flushed between
+    them) and the indexer flops (2 H 128 per visible block and row) against the
+    bf16 tensor peaks.  r = 2 gives k_B = 1024, beyond the fused indexer's 512,
+    so it runs the one-pass scan path (score rows stored, then selected); at 1M
+    that takes seconds per call and is timed only on request."""
+    import torch
+    from block_sparse_long_17_b300.workloads import WORKLOADS, make_prefill
+    out = []
+    for name in ("needle_prefill_32k", "drift_prefill_128k", "needle_prefill_1m"):
+        spec = WORKLOADS[name]
+        wl = make_prefill(spec, dev, indexer_only=True)
+        n = spec.n
+        for r in (2, 4, 8, 16):
+            if r == 2 and n > (1 << 17) and not with_1m_r2:
+                out.append({"workload": name, "r": r, "skipped": "scan path at k_B = 1024: seconds per call at 1M"})
+                continue
+            cfg = qsa.Config(r=r, k_tokens=spec.k_tokens, rope_dims=spec.rope_dims, rope_base=spec.rope_base)
+            nb = n // r
+            kbar = torch.empty((1, nb, spec.d), dtype=torch.bfloat16, device=dev)
+            qsa.qsa_compress_keys(cfg, wl["k_idx"], 0, nb, kbar)
+            q_pos = torch.zeros((1,), dtype=torch.int64, device=dev)
+            idx = torch.empty((1, n, cfg.k_b), dtype=torch.int32, device=dev)
+            cnt = torch.empty((1, n), dtype=torch.int32, device=dev)
+            ws = torch.empty((qsa.qsa_index_topk_workspace(cfg, 1, n, nb),), dtype=torch.uint8, device=dev)
+
+            def step():
+                qsa.qsa_index_topk(cfg, wl["q_idx"], kbar, q_pos, nb, idx, cnt, ws)
+
+            st = 1 if (r == 2 and n > (1 << 17)) else min(steps, 5)
+            ms = _median_step_ms(step, st, min(warmup, 3) if st > 1 else 1, flush)
+            fb = qsa.qsa_index_topk_fallback_rows(cfg, 1, n, nb, ws)
+            i = __import__("numpy").arange(n, dtype="int64")
+            flops = 2 * spec.h_idx * spec.d * int(((i + 1) // r).sum())
+            tf = flops / (ms * 1e-3) / 1e12
+            out.append({"workload": name, "r": r, "k_b": cfg.k_b, "ms": ms, "tflops": tf,
+                        "frac_of_burst": tf / pk["bf16_tflops"], "frac_of_sustained": tf / pk["bf16_tflops_sustained"],
+                        "path": "fused tcgen05" if cfg.k_b <= 512 else "scan (k_B > 512)", "fallback_rows": fb})
+            del kbar, idx, cnt, ws
+            torch.cuda.empty_cache()
+        del wl
+        torch.cuda.empty_cache()
+    assert qsa.qsa_read_device_error() == 0
+    return out
+
+
 def dense_decode_measure(qsa, dspec, dwl, dq, steps: int, warmup: int, dev, flush, hbm_gbs: float,
                          qsa_decode_us: float) -> dict:
     """Dense GQA decode at the decode step's shape, for the pages' form of
@@ -425,6 +474,10 @@ def main():
                     help="multi-token decode workload timed beside the main step, or 'none'")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the chunked-prefill and dense-decode lines timed after the main step")
+    ap.add_argument("--no-index-sweep", action="store_true",
+                    help="skip the indexer timing over micro-block sizes and context lengths")
+    ap.add_argument("--index-sweep-1m-r2", action="store_true",
+                    help="also time r = 2 at 1M in the indexer sweep (seconds per call)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 5 if args.impl == "reference" else 20
@@ -633,6 +686,9 @@ def main():
             line["dense_decode"] = dense_decode_measure(qsa, dspec, dwl, dq, args.steps, args.warmup, dev, flush,
                                                         hbm, decode_ms * 1e3)
         line["dense_prefill"] = dense_prefill_measure(wl, prefill_ms, args.steps, args.warmup, flush)
+    if not args.no_extras and not args.no_index_sweep:
+        line["index_sweep"] = index_sweep_measure(qsa, pk, args.steps, args.warmup, dev, flush,
+                                                  with_1m_r2=args.index_sweep_1m_r2)
     if not args.no_e2e and rank == 0 and do_decode:
         line["e2e"] = e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev)
     if not args.no_cpu_baseline and rank == 0 and do_decode:

@@ -34,7 +34,10 @@ bool valid_config(const qsa_config* c) {
 }
 
 // Shapes the kernels are built for (checked after valid_config).
-bool supported_config(const qsa_config* c) { return c->n_idx_heads == kIdxHeads && c->head_dim == kHeadDim; }
+bool supported_config(const qsa_config* c) {
+  const int h = c->n_idx_heads;
+  return (h == 1 || h == 2 || h == 4 || h == 8) && c->head_dim == kHeadDim;
+}
 
 qsa_status check_config(const qsa_config* c) {
   if (!valid_config(c)) return QSA_ERR_INVALID_ARG;
@@ -68,14 +71,14 @@ struct IndexLayout {
 
 // Workspace: rotated queries, then either the per-CTA selection buffers of the
 // fused indexer (prefill) or one launch's worth of score rows (decode scan).
-IndexLayout index_layout(int64_t B, int64_t n_q, int64_t n_blocks_max, int k_b) {
+IndexLayout index_layout(int64_t B, int64_t n_q, int64_t n_blocks_max, int k_b, int H) {
   IndexLayout L{};
   const int64_t rows = B * n_q;
   L.fused = use_fused_indexer(n_q, k_b);
   L.qt_off = 0;
-  L.s_off = align_up((size_t)rows * kIdxHeads * kHeadDim * sizeof(__nv_bfloat16));
+  L.s_off = align_up((size_t)rows * H * kHeadDim * sizeof(__nv_bfloat16));
   if (L.fused) {
-    L.total = L.s_off + align_up(fused_layout(B, n_q, n_blocks_max).total);
+    L.total = L.s_off + align_up(fused_layout(B, n_q, n_blocks_max, H).total);
     return L;
   }
   L.s_stride = (n_blocks_max + 3) / 4 * 4;
@@ -132,7 +135,7 @@ qsa_status qsa_compress_keys(const qsa_config* cfg, const void* k_idx, int64_t k
 
 size_t qsa_index_topk_workspace(const qsa_config* cfg, int64_t B, int64_t n_q, int64_t n_blocks_max) {
   if (check_config(cfg) != QSA_OK || B < 0 || n_q < 0 || n_blocks_max < 0) return 0;
-  return index_layout(B, n_q, n_blocks_max, k_blocks(cfg)).total;
+  return index_layout(B, n_q, n_blocks_max, k_blocks(cfg), cfg->n_idx_heads).total;
 }
 
 qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* kbar,
@@ -148,35 +151,36 @@ qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* 
   if (!aligned16(q_idx) || (kbar != nullptr && !aligned16(kbar)) || (kbar_stride_b % 8) != 0)
     return QSA_ERR_INVALID_ARG;
   if (B > 1 && kbar_stride_b < n_blocks_max * kHeadDim) return QSA_ERR_INVALID_ARG;
-  const IndexLayout L = index_layout(B, n_q, n_blocks_max, k_blocks(cfg));
+  const IndexLayout L = index_layout(B, n_q, n_blocks_max, k_blocks(cfg), cfg->n_idx_heads);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return QSA_ERR_INVALID_ARG;
   if (ws_bytes < L.total) return QSA_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   __nv_bfloat16* qt = reinterpret_cast<__nv_bfloat16*>(w + L.qt_off);
   float* S = reinterpret_cast<float*>(w + L.s_off);
-  const int r = cfg->r, k_b = k_blocks(cfg);
-  cudaError_t e = launch_rotate_queries(static_cast<const __nv_bfloat16*>(q_idx), q_pos, B, n_q, r,
+  const int r = cfg->r, k_b = k_blocks(cfg), H = cfg->n_idx_heads;
+  const auto* kb = static_cast<const __nv_bfloat16*>(kbar);
+  cudaError_t e = launch_rotate_queries(static_cast<const __nv_bfloat16*>(q_idx), q_pos, B, n_q, r, H,
                                         rope_params(cfg), qt, st);
   if (e != cudaSuccess) return from_cuda(e);
-  if (L.fused) {
-    return from_cuda(launch_index_fused(qt, static_cast<const __nv_bfloat16*>(kbar), kbar_stride_b, q_pos, B,
-                                        n_q, n_blocks_max, r, k_b, idx, count, w + L.s_off, st));
-  }
+  if (L.fused)
+    return from_cuda(launch_index_fused(H, qt, kb, kbar_stride_b, q_pos, B, n_q, n_blocks_max, r, k_b, idx, count,
+                                        w + L.s_off, st));
   const int64_t rows = B * n_q;
   if (n_q <= kDecodeMaxRows && rows <= L.rows_per_launch) {  // decode: one or a few query rows per sequence
-    e = launch_decode_scan(qt, static_cast<const __nv_bfloat16*>(kbar), kbar_stride_b, q_pos, B, (int)n_q, r,
-                           n_blocks_max, S, L.s_stride, st);
+    e = launch_decode_scan(H, qt, kb, kbar_stride_b, q_pos, B, (int)n_q, r, n_blocks_max, S, L.s_stride, st);
     if (e != cudaSuccess) return from_cuda(e);
     return from_cuda(launch_topk_select_cluster(S, L.s_stride, q_pos, n_q, 0, rows, r, k_b, n_blocks_max, idx, count, st));
   }
-  for (int64_t lo = 0; lo < rows; lo += L.rows_per_launch) {
-    const int64_t nr = rows - lo < L.rows_per_launch ? rows - lo : L.rows_per_launch;
-    e = launch_index_scan(qt, static_cast<const __nv_bfloat16*>(kbar), kbar_stride_b, q_pos, n_q, lo,
-                          nr, r, n_blocks_max, S, L.s_stride, st);
-    if (e != cudaSuccess) return from_cuda(e);
-    e = launch_topk_select(S, L.s_stride, q_pos, n_q, lo, nr, r, k_b, n_blocks_max, idx, count, st);
-    if (e != cudaSuccess) return from_cuda(e);
+  // Row ranges within one sequence at a time, as many rows as the score buffer holds.
+  for (int64_t bb = 0; bb < B; ++bb) {
+    for (int64_t j_lo = 0; j_lo < n_q; j_lo += L.rows_per_launch) {
+      const int64_t nr = n_q - j_lo < L.rows_per_launch ? n_q - j_lo : L.rows_per_launch;
+      e = launch_index_scan(H, qt, kb, kbar_stride_b, q_pos, bb, n_q, j_lo, nr, r, n_blocks_max, S, L.s_stride, st);
+      if (e != cudaSuccess) return from_cuda(e);
+      e = launch_topk_select(S, L.s_stride, q_pos, n_q, bb * n_q + j_lo, nr, r, k_b, n_blocks_max, idx, count, st);
+      if (e != cudaSuccess) return from_cuda(e);
+    }
   }
   return QSA_OK;
 }
@@ -188,12 +192,12 @@ qsa_status qsa_index_topk_fallback_rows(const qsa_config* cfg, int64_t B, int64_
   if (B < 0 || n_q < 0 || n_blocks_max < 0 || rows == nullptr) return QSA_ERR_INVALID_ARG;
   *rows = 0;
   if (B == 0 || n_q == 0) return QSA_OK;
-  const IndexLayout L = index_layout(B, n_q, n_blocks_max, k_blocks(cfg));
+  const IndexLayout L = index_layout(B, n_q, n_blocks_max, k_blocks(cfg), cfg->n_idx_heads);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return QSA_ERR_INVALID_ARG;
   if (ws_bytes < L.total) return QSA_ERR_WORKSPACE;
   if (!L.fused) return QSA_OK;  // the scan path selects every row exactly in one pass
-  return from_cuda(read_fused_fallback_rows(static_cast<const char*>(ws) + L.s_off, B, n_q, n_blocks_max, rows,
-                                            reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(read_fused_fallback_rows(static_cast<const char*>(ws) + L.s_off, B, n_q, n_blocks_max,
+                                            cfg->n_idx_heads, rows, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qsa_status qsa_sparse_attn_prefill_impl(const qsa_config* cfg, const void* q, const void* k,

@@ -18,7 +18,7 @@
 namespace qsa {
 
 constexpr int kHeadDim = 128;
-constexpr int kIdxHeads = 4;
+constexpr int kMaxIdxHeads = 8;  // indexer query heads: 1, 2, 4 or 8
 constexpr int kMaxRopePairs = 64;  // rope_dims <= head_dim = 128
 
 // RoPE frequencies computed on the host in fp64: theta_j = base^(-2j/rope_dims).

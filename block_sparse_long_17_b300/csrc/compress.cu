@@ -81,10 +81,10 @@ compress_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_t k_stride_b
 }
 
 // One warp per query token: the RoPE angles of position floor(i / r) are
-// computed once per token and applied to all four indexer heads.
+// computed once per token and applied to all n_heads indexer heads.
 __global__ void __launch_bounds__(kCompressWarps * 32)
 rotate_queries_kernel(const __nv_bfloat16* __restrict__ q_idx, const int64_t* __restrict__ q_pos,
-                      int64_t B, int64_t n_q, int r, RopeParams rope,
+                      int64_t B, int64_t n_q, int r, int n_heads, RopeParams rope,
                       __nv_bfloat16* __restrict__ qt) {
   __shared__ float cs[kCompressWarps][2][kMaxRopePairs];
   __shared__ float row[kCompressWarps][kHeadDim];
@@ -100,9 +100,9 @@ rotate_queries_kernel(const __nv_bfloat16* __restrict__ q_idx, const int64_t* __
     cs[warp][0][j] = c;
     cs[warp][1][j] = s;
   }
-  const __nv_bfloat16* src = q_idx + item * (kIdxHeads * kHeadDim);
-  __nv_bfloat16* dst = qt + item * (kIdxHeads * kHeadDim);
-  for (int h = 0; h < kIdxHeads; ++h) {
+  const __nv_bfloat16* src = q_idx + item * (n_heads * kHeadDim);
+  __nv_bfloat16* dst = qt + item * (n_heads * kHeadDim);
+  for (int h = 0; h < n_heads; ++h) {
     __syncwarp();
 #pragma unroll
     for (int u = 0; u < 4; ++u) row[warp][lane + 32 * u] = __bfloat162float(src[h * kHeadDim + lane + 32 * u]);
@@ -135,12 +135,12 @@ cudaError_t launch_compress_keys(const __nv_bfloat16* k_idx, int64_t k_stride_b,
 }
 
 cudaError_t launch_rotate_queries(const __nv_bfloat16* q_idx, const int64_t* q_pos, int64_t B,
-                                  int64_t n_q, int r, const RopeParams& rope, __nv_bfloat16* qt,
+                                  int64_t n_q, int r, int n_heads, const RopeParams& rope, __nv_bfloat16* qt,
                                   cudaStream_t st) {
   const int64_t items = B * n_q;
   if (items == 0) return cudaSuccess;
   const int64_t grid = (items + kCompressWarps - 1) / kCompressWarps;
-  rotate_queries_kernel<<<(unsigned)grid, kCompressWarps * 32, 0, st>>>(q_idx, q_pos, B, n_q, r,
+  rotate_queries_kernel<<<(unsigned)grid, kCompressWarps * 32, 0, st>>>(q_idx, q_pos, B, n_q, r, n_heads,
                                                                          rope, qt);
   return count_launch(cudaGetLastError());
 }

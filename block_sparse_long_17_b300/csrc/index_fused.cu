@@ -51,8 +51,8 @@
 
 namespace qsa {
 
-constexpr int kTT = 48;                  // query tokens per tile
-constexpr int kNRows = kTT * kIdxHeads;  // 192: MMA N (token, head rows)
+constexpr int kTT = 48;                  // query tokens per tile (most; 24 with 8 indexer heads)
+constexpr int kNRows = 192;              // largest MMA N (token, head rows) of a tile
 constexpr int kMB = 128;                 // blocks per chunk: MMA M
 constexpr int kAStages = 3;              // kbar TMA ring depth
 constexpr int kEpiWarps = 12;            // 3 per TMEM lane quarter, 16 tokens each
@@ -73,7 +73,22 @@ constexpr int kFbCtas = 148;             // fallback kernel CTAs (one row each a
 constexpr int kTilesPerLaunch = 1024;    // tiles per fused launch (bounds the row buffers: 1.9 GiB)
 constexpr int kFinKWarps = 4;            // warps per CTA of the finalize kernel
 constexpr uint32_t kABytes = kMB * 128 * 2;     // 32 KB
-constexpr uint32_t kBBytes = kNRows * 128 * 2;  // 48 KB
+
+// Tile shape for H indexer heads: TT query tokens, NR = TT H MMA columns
+// (token-major, the H heads of a token adjacent), TPW tokens and CPW = TPW H
+// accumulator columns per score warp (three warps per TMEM lane quarter).
+template <int H>
+struct FusedShape {
+  static constexpr int TT = H == 8 ? 24 : 48;
+  static constexpr int NR = TT * H;
+  static constexpr int TPW = TT / 3;
+  static constexpr int CPW = TPW * H;
+  static constexpr uint32_t BBytes = NR * 128 * 2;
+  static_assert(NR % 16 == 0 && NR <= kNRows && TPW % 4 == 0, "tile shape");
+};
+
+// Tokens per tile for H indexer heads (host and device).
+__host__ __device__ constexpr int fused_tile_tokens(int H) { return H == 8 ? 24 : 48; }
 
 struct FusedSmem {
   uint8_t a[kAStages][2][kMB * 128];   // kbar chunk, dims 0-63 | 64-127 (SW128)
@@ -105,13 +120,14 @@ constexpr int kPilotMin = 2048;    // at least this many pilot samples per row w
 constexpr int kPilotNum = 8;       // tau aims at kPilotNum / kPilotDen x k_B entries per row:
 constexpr int kPilotDen = 5;       // near the middle, in ratio, of the accepted [k_B, 2.5 k_B]
 
+template <int TT>
 __device__ __forceinline__ TileMeta tile_meta(int64_t t, int64_t tiles_per_seq, int64_t n_q,
                                               const int64_t* q_pos, int rshift, int k_b, int64_t c_cap) {
   TileMeta m;
   m.bb = t / tiles_per_seq;
-  m.tok0 = (t % tiles_per_seq) * kTT;
+  m.tok0 = (t % tiles_per_seq) * TT;
   const int64_t rem = n_q - m.tok0;
-  m.nvalid = rem < kTT ? (int)rem : kTT;
+  m.nvalid = rem < TT ? (int)rem : TT;
   m.i0 = q_pos[m.bb] + m.tok0;
   int64_t c = (m.i0 + m.nvalid) >> rshift;
   if (c > c_cap) c = c_cap;
@@ -387,12 +403,15 @@ __device__ __forceinline__ int64_t tile_order(int64_t k, int64_t t_count) {
   return kk < t_count ? t_count - 1 - kk : -1;
 }
 
+template <int H>
 __global__ void __launch_bounds__(kFThreads, 1)
 index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_kp, const int64_t* __restrict__ q_pos,
                         int64_t n_q, int64_t tiles_per_seq, int64_t t_begin, int64_t t_count, int rshift,
                         int k_b, int64_t c_cap, uint2* __restrict__ buf, int* __restrict__ cnt) {
   using namespace sm100;
+  using Sh = FusedShape<H>;
+  constexpr int TT = Sh::TT, TPW = Sh::TPW, CPW = Sh::CPW;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* const smem_base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   FusedSmem& S = *reinterpret_cast<FusedSmem*>(smem_base);
@@ -417,7 +436,7 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     S.abort_flag = 0;
     fence_mbar_init();
   }
-  for (int j = threadIdx.x; j < kTT * (kPBins / 2); j += kFThreads) (&S.phist[0][0])[j] = 0;
+  for (int j = threadIdx.x; j < TT * (kPBins / 2); j += kFThreads) (&S.phist[0][0])[j] = 0;
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
@@ -440,12 +459,12 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       for (int64_t k = 0; ok && k < rounds; ++k) {
         const int64_t lt = tile_order(k, t_count);
         if (lt < 0) continue;
-        const TileMeta m = tile_meta(t_begin + lt, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
+        const TileMeta m = tile_meta<TT>(t_begin + lt, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
         if (!m.mma) continue;
         if (!mbar_wait(&S.b_empty, (b_uses & 1) ^ 1, abort_flag, kWaitCycles, 128)) { ok = false; break; }
         ++b_uses;
-        mbar_arrive_expect_tx(&S.b_full, kBBytes);
-        const int qrow = (int)((m.bb * n_q + m.tok0) * kIdxHeads);
+        mbar_arrive_expect_tx(&S.b_full, Sh::BBytes);
+        const int qrow = (int)((m.bb * n_q + m.tok0) * H);
         tma_load_2d(S.b[0], &tm_q, &S.b_full, 0, qrow);
         tma_load_2d(S.b[1], &tm_q, &S.b_full, 64, qrow);
         const int total = m.npilot + m.nchunks;
@@ -478,14 +497,14 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kMB, kNRows);
+      constexpr uint32_t idesc = idesc_bf16_f32(kMB, Sh::NR);
       uint32_t it = 0, ct = 0, b_uses = 0;
       bool ok = true;
       const uint32_t b0 = smem_u32(S.b[0]), b1 = smem_u32(S.b[1]);
       for (int64_t k = 0; ok && k < rounds; ++k) {
         const int64_t lt = tile_order(k, t_count);
         if (lt < 0) continue;
-        const TileMeta m = tile_meta(t_begin + lt, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
+        const TileMeta m = tile_meta<TT>(t_begin + lt, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
         if (!m.mma) continue;
         if (!mbar_wait(&S.b_full, b_uses & 1, abort_flag, kWaitCycles, 64)) { ok = false; break; }
         ++b_uses;
@@ -516,29 +535,29 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     }
   } else {
     // ------------------------------------------------------------ score warps
-    const int ew = warp - 2;            // 0..15
+    const int ew = warp - 2;            // 0..11
     const int q4 = warp & 3;            // TMEM lane quarter: blocks 32 q4 .. 32 q4 + 31 of a chunk
-    const int h = ew >> 2;              // tokens 16 h .. 16 h + 15 (TMEM columns 64 h .. 64 h + 63)
+    const int h = ew >> 2;              // tokens TPW h .. TPW h + TPW - 1 (TMEM columns CPW h ..)
     const int cap32 = (int)(c_cap < 0x7fffffff ? c_cap : 0x7fffffff);
     uint32_t ct = 0, pilot_n = 0;
     bool ok = true;
     for (int64_t k = 0; ok && k < rounds; ++k) {
       const int64_t lt = tile_order(k, t_count);
       if (lt < 0) continue;
-      const TileMeta m = tile_meta(t_begin + lt, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
+      const TileMeta m = tile_meta<TT>(t_begin + lt, tiles_per_seq, n_q, q_pos, rshift, k_b, c_cap);
       if (!m.mma) continue;
-      // Token 16 h + j sits at position pos16 + j.
-      const int pos16 = (int)(m.i0 + 16 * h);
-      const int cmin16 = min((pos16 + 1) >> rshift, cap32);  // smallest c of the warp's tokens
-      // Segment of (token 16 h + j, this warp's lane quarter): seg0 + j * 4 kSeg.
-      uint2* const seg0 = buf + ((lt * kTT + 16 * h) * 4 + q4) * kSeg;
-      // Thresholds and entry counts of the warp's 16 tokens (the same in every lane).
-      uint32_t tau16[16];
-      int cnt16[16];
+      // Token TPW h + j sits at position posw + j.
+      const int posw = (int)(m.i0 + TPW * h);
+      const int cminw = min((posw + 1) >> rshift, cap32);  // smallest c of the warp's tokens
+      // Segment of (token TPW h + j, this warp's lane quarter): seg0 + j * 4 kSeg.
+      uint2* const seg0 = buf + ((lt * TT + TPW * h) * 4 + q4) * kSeg;
+      // Thresholds and entry counts of the warp's tokens (the same in every lane).
+      uint32_t tauw[TPW];
+      int cntw[TPW];
 #pragma unroll
-      for (int k2 = 0; k2 < 16; ++k2) {
-        tau16[k2] = 0xffffffffu;
-        cnt16[k2] = 0;
+      for (int k2 = 0; k2 < TPW; ++k2) {
+        tauw[k2] = 0xffffffffu;
+        cntw[k2] = 0;
       }
       const int total = m.npilot + m.nchunks;
       for (int x = 0; x < total; ++x, ++ct) {
@@ -549,7 +568,7 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           if (lane == 0) mbar_arrive(&S.pilot_bar);
           if (!warp_wait(&S.pilot_bar, pilot_n & 1, abort_flag)) { ok = false; break; }
 #pragma unroll 1
-          for (int t = ew; t < kTT; t += kEpiWarps) {
+          for (int t = ew; t < TT; t += kEpiWarps) {
             const int64_t c = token_c(m, t, rshift, c_cap);
             // Rows that do not select (past the end, or c <= k_B) collect nothing.
             const uint32_t tau = pilot_tau(S.phist[t], c, k_b);
@@ -559,12 +578,12 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           if (lane == 0) mbar_arrive(&S.tau_bar);
           if (!warp_wait(&S.tau_bar, pilot_n & 1, abort_flag)) { ok = false; break; }
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const uint4 t4 = *reinterpret_cast<const uint4*>(&S.tau[16 * h + 4 * k4]);
-            tau16[4 * k4] = t4.x;
-            tau16[4 * k4 + 1] = t4.y;
-            tau16[4 * k4 + 2] = t4.z;
-            tau16[4 * k4 + 3] = t4.w;
+          for (int k4 = 0; k4 < TPW / 4; ++k4) {
+            const uint4 t4 = *reinterpret_cast<const uint4*>(&S.tau[TPW * h + 4 * k4]);
+            tauw[4 * k4] = t4.x;
+            tauw[4 * k4 + 1] = t4.y;
+            tauw[4 * k4 + 2] = t4.z;
+            tauw[4 * k4 + 3] = t4.w;
           }
           ++pilot_n;
         }
@@ -572,34 +591,62 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         if (!warp_wait(&S.tfull[acc], (ct >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
 
-        // The 64 accumulator columns of this warp's 16 tokens are reduced to
-        // 16 scores in registers (32 columns at a time), and the accumulator is
-        // handed back to the MMA warp at once.  x + |x| is 2 ReLU(x) exactly and
-        // doubling commutes with the rounding of the sums, so the bit patterns
-        // of 2 x score order exactly as the scores do.
-        uint32_t u16[16];
+        // The CPW accumulator columns of this warp's TPW tokens are reduced to
+        // TPW scores in registers, and the accumulator is handed back to the
+        // MMA warp at once.  x + |x| is 2 ReLU(x) exactly and doubling
+        // commutes with the rounding of the sums, so the bit patterns of
+        // 2 x score order exactly as the scores do.
+        uint32_t uw[TPW];
         {
-          const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)acc * kAccCols + (uint32_t)(64 * h);
+          const uint32_t taddr = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)acc * kAccCols + (uint32_t)(CPW * h);
+          if constexpr (H == 4) {
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
-            uint32_t v[32];
-            tmem_ld32(taddr + (uint32_t)(32 * g), v);
+            for (int g = 0; g < 2; ++g) {
+              uint32_t v[32];
+              tmem_ld32(taddr + (uint32_t)(32 * g), v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int kk = 0; kk < 8; kk += 2) {  // two tokens at a time: packed fp32 pair adds
+                float rr[2][4];
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+#pragma unroll
+                  for (int hh = 0; hh < 4; ++hh) {
+                    const float a = __uint_as_float(v[4 * (kk + e) + hh]);
+                    rr[e][hh] = a + fabsf(a);
+                  }
+                const float2 s01 = __fadd2_rn(make_float2(rr[0][0], rr[1][0]), make_float2(rr[0][1], rr[1][1]));
+                const float2 s23 = __fadd2_rn(make_float2(rr[0][2], rr[1][2]), make_float2(rr[0][3], rr[1][3]));
+                const float2 tot = __fadd2_rn(s01, s23);
+                uw[8 * g + kk] = __float_as_uint(tot.x);
+                uw[8 * g + kk + 1] = __float_as_uint(tot.y);
+              }
+            }
+          } else if constexpr (CPW == 16) {  // one head: 16 columns, one per token
+            uint32_t v[16];
+            tmem_ld16(taddr, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int kk = 0; kk < 8; kk += 2) {  // two tokens at a time: packed fp32 pair adds
-              float rr[2][4];
+            for (int k2 = 0; k2 < TPW; ++k2) {
+              const float a = __uint_as_float(v[k2]);
+              uw[k2] = __float_as_uint(a + fabsf(a));
+            }
+          } else {  // 32 columns per load: 32 / H tokens of H heads, summed in head order
 #pragma unroll
-              for (int e = 0; e < 2; ++e)
+            for (int g = 0; g < CPW / 32; ++g) {
+              uint32_t v[32];
+              tmem_ld32(taddr + (uint32_t)(32 * g), v);
+              tmem_ld_wait();
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                  const float a = __uint_as_float(v[4 * (kk + e) + hh]);
-                  rr[e][hh] = a + fabsf(a);
+              for (int kk = 0; kk < 32 / H; ++kk) {
+                float sum = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < H; ++hh) {
+                  const float a = __uint_as_float(v[H * kk + hh]);
+                  sum += a + fabsf(a);
                 }
-              const float2 s01 = __fadd2_rn(make_float2(rr[0][0], rr[1][0]), make_float2(rr[0][1], rr[1][1]));
-              const float2 s23 = __fadd2_rn(make_float2(rr[0][2], rr[1][2]), make_float2(rr[0][3], rr[1][3]));
-              const float2 tot = __fadd2_rn(s01, s23);
-              u16[8 * g + kk] = __float_as_uint(tot.x);
-              u16[8 * g + kk + 1] = __float_as_uint(tot.y);
+                uw[(32 / H) * g + kk] = __float_as_uint(sum);
+              }
             }
           }
           tc_fence_before();
@@ -612,16 +659,16 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         const int ph = pilot ? x / m.mc : 0;
         const int gbase = pilot ? (x % m.mc) * kMB + 32 * q4 : q4 * (m.nchunks * 32) + (x - m.npilot) * 32;
         const int bi = pilot ? (gbase + lane) * kPilotStride + ph : gbase + lane;
-        // Every block of the warp is visible to all 16 tokens when they end
+        // Every block of the warp is visible to all its tokens when they end
         // below the first token's visible range.
         const int warp_last = pilot ? (m.mc * kMB) * kPilotStride : gbase + 32;
-        const bool chunk_all_visible = warp_last <= cmin16;
-        // Lanes (blocks) token 16 h + k2 sees in a main chunk: a prefix of the
+        const bool chunk_all_visible = warp_last <= cminw;
+        // Lanes (blocks) token TPW h + k2 sees in a main chunk: a prefix of the
         // warp, as block ids grow with the lane.  Tokens that do not select are
         // excluded by their threshold.
         auto vis_mask = [&](int k2) -> unsigned {
           if (chunk_all_visible) return 0xffffffffu;
-          int c = (pos16 + k2 + 1) >> rshift;
+          int c = (posw + k2 + 1) >> rshift;
           c = c < cap32 ? c : cap32;
           const int lim = c - gbase;
           return lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : (1u << lim) - 1u);
@@ -633,10 +680,10 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           // collect pass applies each row's exact range.
           if (gbase + lane < m.ngroups) {
 #pragma unroll
-            for (int k2 = 0; k2 < 16; ++k2) {
-              int bin = (int)(u16[k2] >> kPShift) - kPBase;
+            for (int k2 = 0; k2 < TPW; ++k2) {
+              int bin = (int)(uw[k2] >> kPShift) - kPBase;
               bin = bin < 0 ? 0 : (bin > kPBins - 1 ? kPBins - 1 : bin);
-              atomicAdd(&S.phist[16 * h + k2][bin >> 1], (bin & 1) ? 65536u : 1u);
+              atomicAdd(&S.phist[TPW * h + k2][bin >> 1], (bin & 1) ? 65536u : 1u);
             }
           }
         } else {
@@ -644,22 +691,22 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             const unsigned lt_mask = (1u << lane) - 1u;
             if (chunk_all_visible) {
 #pragma unroll
-              for (int k2 = 0; k2 < 16; ++k2) {
-                const bool mine = u16[k2] >= tau16[k2];
+              for (int k2 = 0; k2 < TPW; ++k2) {
+                const bool mine = uw[k2] >= tauw[k2];
                 const unsigned tmk = __ballot_sync(0xffffffffu, mine);
                 // An overflowing segment writes its last slot; its count keeps
                 // growing, and the finalize sends such a row to the fallback.
-                const int pos = min(cnt16[k2] + __popc(tmk & lt_mask), kSeg - 1);
-                if (mine) seg0[k2 * 4 * kSeg + pos] = make_uint2(u16[k2], (uint32_t)bi);
-                cnt16[k2] += __popc(tmk);
+                const int pos = min(cntw[k2] + __popc(tmk & lt_mask), kSeg - 1);
+                if (mine) seg0[k2 * 4 * kSeg + pos] = make_uint2(uw[k2], (uint32_t)bi);
+                cntw[k2] += __popc(tmk);
               }
             } else {
 #pragma unroll
-              for (int k2 = 0; k2 < 16; ++k2) {
-                const unsigned tmk = __ballot_sync(0xffffffffu, u16[k2] >= tau16[k2]) & vis_mask(k2);
-                const int pos = min(cnt16[k2] + __popc(tmk & lt_mask), kSeg - 1);
-                if ((tmk >> lane) & 1u) seg0[k2 * 4 * kSeg + pos] = make_uint2(u16[k2], (uint32_t)bi);
-                cnt16[k2] += __popc(tmk);
+              for (int k2 = 0; k2 < TPW; ++k2) {
+                const unsigned tmk = __ballot_sync(0xffffffffu, uw[k2] >= tauw[k2]) & vis_mask(k2);
+                const int pos = min(cntw[k2] + __popc(tmk & lt_mask), kSeg - 1);
+                if ((tmk >> lane) & 1u) seg0[k2 * 4 * kSeg + pos] = make_uint2(uw[k2], (uint32_t)bi);
+                cntw[k2] += __popc(tmk);
               }
             }
           }
@@ -668,10 +715,10 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       if (!ok) break;
       // ---- tile done: this warp's entry counts go to the finalize kernel
       if (lane == 0) {
-        int4* const dst = reinterpret_cast<int4*>(cnt + (lt * 4 + q4) * kTT + 16 * h);
+        int4* const dst = reinterpret_cast<int4*>(cnt + (lt * 4 + q4) * TT + TPW * h);
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4)
-          dst[k4] = make_int4(cnt16[4 * k4], cnt16[4 * k4 + 1], cnt16[4 * k4 + 2], cnt16[4 * k4 + 3]);
+        for (int k4 = 0; k4 < TPW / 4; ++k4)
+          dst[k4] = make_int4(cntw[4 * k4], cntw[4 * k4 + 1], cntw[4 * k4 + 2], cntw[4 * k4 + 3]);
       }
       __syncwarp();
     }
@@ -694,18 +741,18 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 __global__ void __launch_bounds__(32 * kFinKWarps, 4)
 index_finalize_kernel(const uint2* __restrict__ buf, const int* __restrict__ cnt, const int64_t* __restrict__ q_pos,
                       int64_t n_q, int64_t tiles_per_seq, int64_t t_begin, int64_t t_count, int rshift, int k_b,
-                      int64_t c_cap, int32_t* __restrict__ idx, int32_t* __restrict__ count,
+                      int64_t c_cap, int tt, int32_t* __restrict__ idx, int32_t* __restrict__ count,
                       int64_t* __restrict__ fb_rows, int* __restrict__ fb_count) {
   __shared__ __align__(16) uint32_t hist[kFinKWarps][512];
   __shared__ int32_t ids[kFinKWarps][kFCap];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t rows = t_count * kTT;
+  const int64_t rows = t_count * tt;  // tt: tokens per tile
   for (int64_t rr = (int64_t)blockIdx.x * kFinKWarps + w; rr < rows; rr += (int64_t)gridDim.x * kFinKWarps) {
-    const int64_t lt = rr / kTT;
-    const int t = (int)(rr % kTT);
+    const int64_t lt = rr / tt;
+    const int t = (int)(rr % tt);
     const int64_t tile = t_begin + lt;
     const int64_t bb = tile / tiles_per_seq;
-    const int64_t tok = (tile % tiles_per_seq) * kTT + t;
+    const int64_t tok = (tile % tiles_per_seq) * tt + t;
     if (tok >= n_q) continue;
     int64_t c = (q_pos[bb] + tok + 1) >> rshift;
     if (c > c_cap) c = c_cap;
@@ -716,12 +763,12 @@ index_finalize_kernel(const uint2* __restrict__ buf, const int* __restrict__ cnt
       if (lane == 0) count[grow] = (int32_t)c;
       continue;
     }
-    const int* const cr = cnt + lt * 4 * kTT + t;
-    const int n0 = cr[0], n1 = cr[kTT], n2 = cr[2 * kTT], n3 = cr[3 * kTT];
+    const int* const cr = cnt + lt * 4 * tt + t;
+    const int n0 = cr[0], n1 = cr[tt], n2 = cr[2 * tt], n3 = cr[3 * tt];
     const int n = n0 + n1 + n2 + n3;
     const bool seg_ok = n0 <= kSeg && n1 <= kSeg && n2 <= kSeg && n3 <= kSeg;
     if (seg_ok && n >= k_b && n <= kFCap) {
-      finalize_row(buf + (lt * kTT + t) * 4 * kSeg, n0, n0 + n1, n0 + n1 + n2, n, k_b, hist[w], ids[w], out);
+      finalize_row(buf + (lt * tt + t) * 4 * kSeg, n0, n0 + n1, n0 + n1 + n2, n, k_b, hist[w], ids[w], out);
       if (lane == 0) count[grow] = k_b;
     } else if (lane == 0) {
       fb_rows[atomicAdd(fb_count, 1)] = grow;  // the exact fallback kernel takes it
@@ -731,12 +778,13 @@ index_finalize_kernel(const uint2* __restrict__ buf, const int* __restrict__ cnt
 
 // ---------------------------------------------------------------------------------------------
 // Exact fallback for rows whose threshold missed: one CTA scores the whole row
-// (m16n8k16 MMAs on kbar rows read straight from memory, the 4 heads in the MMA
-// columns) into its scratch row, then runs the CTA radix selection on it.
+// (m16n8k16 MMAs on kbar rows read straight from memory, the n_heads indexer
+// heads in the MMA columns) into its scratch row, then runs the CTA radix
+// selection on it.
 __global__ void __launch_bounds__(kSelThreads)
 index_fallback_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16* __restrict__ kbar,
                       int64_t kbar_stride_b, const int64_t* __restrict__ q_pos, int64_t n_q, int r, int k_b,
-                      int64_t c_cap, const int64_t* __restrict__ fb_rows, const int* __restrict__ fb_count,
+                      int n_heads, int64_t c_cap, const int64_t* __restrict__ fb_rows, const int* __restrict__ fb_count,
                       float* __restrict__ scratch, int64_t scratch_stride, int32_t* __restrict__ idx,
                       int32_t* __restrict__ count) {
   __shared__ SelectSmem sm;
@@ -749,13 +797,14 @@ index_fallback_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16*
     const int64_t bb = row / n_q;
     int64_t c = (q_pos[bb] + row % n_q + 1) / r;
     if (c > c_cap) c = c_cap;
-    // B fragment: columns gid < 4 are the 4 heads, the others zero.
+    // B fragment: columns gid < n_heads are the heads, the others zero.
     uint32_t qf[16];
     {
-      const uint4* src = reinterpret_cast<const uint4*>(qt + (row * kIdxHeads + (gid & 3)) * kHeadDim + 32 * t);
+      const int hh = gid < n_heads ? gid : 0;
+      const uint4* src = reinterpret_cast<const uint4*>(qt + (row * n_heads + hh) * kHeadDim + 32 * t);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const uint4 v = gid < 4 ? src[u] : make_uint4(0, 0, 0, 0);
+        const uint4 v = gid < n_heads ? src[u] : make_uint4(0, 0, 0, 0);
         qf[4 * u] = v.x; qf[4 * u + 1] = v.y; qf[4 * u + 2] = v.z; qf[4 * u + 3] = v.w;
       }
     }
@@ -779,11 +828,14 @@ index_fallback_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16*
         const uint32_t bq[2] = {qf[2 * ks], qf[2 * ks + 1]};
         mma_bf16_16816(acc, a, bq);
       }
-      // acc: (block b0+gid, heads 2t, 2t+1), (b0+gid+8, heads 2t, 2t+1); heads >= 4 are zero.
+      // acc: (block b0+gid, heads 2t, 2t+1), (b0+gid+8, heads 2t, 2t+1); heads >=
+      // n_heads are zero, so the sum over all 8 columns is the sum over the heads.
       float sa = fmaxf(acc[0], 0.f) + fmaxf(acc[1], 0.f);
       float sb = fmaxf(acc[2], 0.f) + fmaxf(acc[3], 0.f);
       sa += __shfl_xor_sync(0xffffffffu, sa, 1);
       sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+      sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+      sb += __shfl_xor_sync(0xffffffffu, sb, 2);
       if (t == 0 && b0 + gid < c) s[b0 + gid] = sa;
       if (t == 0 && b0 + gid + 8 < c) s[b0 + gid + 8] = sb;
     }
@@ -806,15 +858,16 @@ struct FusedLayout {
 // Workspace of the fused path (after the rotated queries): the entry buffers of
 // one launch's tiles (48 tokens x 4 segments x kSeg entries per tile) and their
 // counts, the fallback row list and counter, and the fallback kernel's score rows.
-inline FusedLayout fused_layout(int64_t B, int64_t n_q, int64_t n_blocks_max) {
+inline FusedLayout fused_layout(int64_t B, int64_t n_q, int64_t n_blocks_max, int H) {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
+  const int tt = fused_tile_tokens(H);
   FusedLayout L;
-  L.tiles_per_seq = (n_q + kTT - 1) / kTT;
+  L.tiles_per_seq = (n_q + tt - 1) / tt;
   L.n_tiles = B * L.tiles_per_seq;
   L.tiles_per_launch = L.n_tiles < kTilesPerLaunch ? L.n_tiles : kTilesPerLaunch;
   L.buf_off = 0;
-  L.cnt_off = al(L.buf_off + (size_t)L.tiles_per_launch * kTT * 4 * kSeg * sizeof(uint2));
-  L.fb_rows_off = al(L.cnt_off + (size_t)L.tiles_per_launch * 4 * kTT * sizeof(int));
+  L.cnt_off = al(L.buf_off + (size_t)L.tiles_per_launch * tt * 4 * kSeg * sizeof(uint2));
+  L.fb_rows_off = al(L.cnt_off + (size_t)L.tiles_per_launch * 4 * tt * sizeof(int));
   L.fb_count_off = al(L.fb_rows_off + (size_t)B * n_q * sizeof(int64_t));
   L.scratch_off = al(L.fb_count_off + sizeof(int));
   L.scratch_stride = (n_blocks_max + 63) / 64 * 64;
@@ -839,19 +892,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kbar, int64_t kbar_stride_b,
+cudaError_t launch_index_fused(int H, const __nv_bfloat16* qt, const __nv_bfloat16* kbar, int64_t kbar_stride_b,
                                const int64_t* q_pos, int64_t B, int64_t n_q, int64_t n_blocks_max, int r,
                                int k_b, int32_t* idx, int32_t* count, void* ws, cudaStream_t st) {
-  const FusedLayout L = fused_layout(B, n_q, n_blocks_max);
+  if (H != 1 && H != 2 && H != 4 && H != 8) return cudaErrorInvalidValue;
+  const FusedLayout L = fused_layout(B, n_q, n_blocks_max, H);
+  const int tt = fused_tile_tokens(H);
   if (L.n_tiles == 0) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   char* w = static_cast<char*>(ws);
   CUtensorMap tm_q, tm_k;
   {
-    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)(B * n_q * kIdxHeads)};
+    const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)(B * n_q * H)};
     const cuuint64_t strides[1] = {kHeadDim * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)kNRows};
+    const cuuint32_t box[2] = {64, (cuuint32_t)(tt * H)};
     const cuuint32_t estr[2] = {1, 1};
     if (encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(qt), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -889,7 +944,11 @@ cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kba
       return cudaErrorInvalidValue;
   }
   {
-    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(index_topk_fused_kernel), (int)kFusedSmemBytes);
+    const void* kern = H == 1   ? reinterpret_cast<const void*>(index_topk_fused_kernel<1>)
+                       : H == 2 ? reinterpret_cast<const void*>(index_topk_fused_kernel<2>)
+                       : H == 4 ? reinterpret_cast<const void*>(index_topk_fused_kernel<4>)
+                                : reinterpret_cast<const void*>(index_topk_fused_kernel<8>);
+    cudaError_t e = ensure_dyn_smem(kern, (int)kFusedSmemBytes);
     if (e != cudaSuccess) return e;
   }
   int* fb_count = reinterpret_cast<int*>(w + L.fb_count_off);
@@ -909,19 +968,27 @@ cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kba
     const int64_t t_count = t_end - t_begin;
     int64_t grid = sms < kFMaxCtas ? sms : kFMaxCtas;
     if (grid > t_count) grid = t_count;
-    index_topk_fused_kernel<<<(unsigned)grid, kFThreads, kFusedSmemBytes, st>>>(
-        tm_q, tm_k, tm_kp, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, n_blocks_max, buf, cnt);
+#define QSA_FUSED_LAUNCH(HH)                                                                                 \
+  index_topk_fused_kernel<HH><<<(unsigned)grid, kFThreads, kFusedSmemBytes, st>>>(                           \
+      tm_q, tm_k, tm_kp, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, n_blocks_max, buf, cnt)
+    switch (H) {
+      case 1: QSA_FUSED_LAUNCH(1); break;
+      case 2: QSA_FUSED_LAUNCH(2); break;
+      case 4: QSA_FUSED_LAUNCH(4); break;
+      default: QSA_FUSED_LAUNCH(8); break;
+    }
+#undef QSA_FUSED_LAUNCH
     e = count_launch(cudaGetLastError());
     if (e != cudaSuccess) return e;
-    const int64_t fin_blocks = (t_count * kTT + kFinKWarps - 1) / kFinKWarps;
+    const int64_t fin_blocks = (t_count * tt + kFinKWarps - 1) / kFinKWarps;
     index_finalize_kernel<<<(unsigned)fin_blocks, 32 * kFinKWarps, 0, st>>>(
-        buf, cnt, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, n_blocks_max, idx, count, fb_rows,
+        buf, cnt, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, n_blocks_max, tt, idx, count, fb_rows,
         fb_count);
     e = count_launch(cudaGetLastError());
     if (e != cudaSuccess) return e;
   }
   index_fallback_kernel<<<kFbCtas, kSelThreads, 0, st>>>(
-      qt, kbar, kbar_stride_b, q_pos, n_q, r, k_b, n_blocks_max, fb_rows, fb_count,
+      qt, kbar, kbar_stride_b, q_pos, n_q, r, k_b, H, n_blocks_max, fb_rows, fb_count,
       reinterpret_cast<float*>(w + L.scratch_off), L.scratch_stride, idx, count);
   return count_launch(cudaGetLastError());
 }
@@ -929,9 +996,9 @@ cudaError_t launch_index_fused(const __nv_bfloat16* qt, const __nv_bfloat16* kba
 
 // Rows of the last fused-indexer call on workspace `ws` (its fused part) that
 // went to the exact fallback kernel.  Waits for `st`.
-inline cudaError_t read_fused_fallback_rows(const void* ws, int64_t B, int64_t n_q, int64_t n_blocks_max,
+inline cudaError_t read_fused_fallback_rows(const void* ws, int64_t B, int64_t n_q, int64_t n_blocks_max, int H,
                                             int64_t* rows, cudaStream_t st) {
-  const FusedLayout L = fused_layout(B, n_q, n_blocks_max);
+  const FusedLayout L = fused_layout(B, n_q, n_blocks_max, H);
   int n = 0;
   cudaError_t e = cudaMemcpyAsync(&n, static_cast<const char*>(ws) + L.fb_count_off, sizeof(int),
                                   cudaMemcpyDeviceToHost, st);

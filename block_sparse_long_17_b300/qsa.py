@@ -161,7 +161,7 @@ def qsa_index_topk_workspace(cfg: Config, B: int, n_q: int, n_blocks_max: int) -
 def qsa_index_topk(cfg: Config, q_idx: torch.Tensor, kbar: torch.Tensor, q_pos: torch.Tensor,
                    n_blocks_max: int, idx: torch.Tensor, count: torch.Tensor, ws: torch.Tensor,
                    stream=None) -> None:
-    """q_idx [B, n_q, 4, d] bf16; kbar [B, N_cap, d] bf16; q_pos [B] int64 (device);
+    """q_idx [B, n_q, n_idx_heads, d] bf16; kbar [B, N_cap, d] bf16; q_pos [B] int64 (device);
     idx [B, n_q, k_B] int32; count [B, n_q] int32; ws: uint8 workspace."""
     _bf16(q_idx, "q_idx"); _bf16(kbar, "kbar"); _i64(q_pos, "q_pos")
     for t, nm in ((idx, "idx"), (count, "count")):
@@ -348,7 +348,7 @@ class QsaDecode:
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=device)
 
     def __call__(self, q_idx, q, kbar, k_cache, v_cache, cache_len, stream=None, with_lse=True):
-        """q_idx [B, 1, 4, d]; q [B, Hq, d]; cache_len [B] int64 including the new token."""
+        """q_idx [B, 1, n_idx_heads, d]; q [B, Hq, d]; cache_len [B] int64 including the new token."""
         q_pos = cache_len - 1
         qsa_index_topk(self.cfg, q_idx, kbar, q_pos, self.n_blocks_max, self.idx, self.count,
                        self.ws_idx, stream)

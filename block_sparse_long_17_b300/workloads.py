@@ -110,17 +110,21 @@ def _ar1_drift(n: int, width: int, rng: np.random.Generator, rho: float = 0.99) 
     return lfilter([np.sqrt(1.0 - rho * rho)], [1.0, -rho], eps, axis=0)
 
 
-def make_prefill(spec: PrefillSpec, device="cpu", *, n: int | None = None) -> dict:
-    """Draw one prefill workload.  `n` overrides the sequence length (smaller test cases)."""
+def make_prefill(spec: PrefillSpec, device="cpu", *, n: int | None = None, indexer_only: bool = False) -> dict:
+    """Draw one prefill workload.  `n` overrides the sequence length (smaller test cases).
+    indexer_only: draw only q_idx and k_idx (the first two draws, so their values
+    are those of the full workload); q, k, v are None."""
     n = spec.n if n is None else n
     B, d = spec.batch, spec.d
     gen = torch.Generator(device=device)
     gen.manual_seed(spec.seed)
     q_idx = _randn_bf16((B, n, spec.h_idx, d), gen, device)
     k_idx = _randn_bf16((B, n, d), gen, device)
-    q = _randn_bf16((B, n, spec.hq, d), gen, device)
-    k = _randn_bf16((B, spec.hkv, n, d), gen, device)
-    v = _randn_bf16((B, spec.hkv, n, d), gen, device)
+    q = k = v = None
+    if not indexer_only:
+        q = _randn_bf16((B, n, spec.hq, d), gen, device)
+        k = _randn_bf16((B, spec.hkv, n, d), gen, device)
+        v = _randn_bf16((B, spec.hkv, n, d), gen, device)
     needles = []
     if spec.needles:
         rng = np.random.default_rng(spec.seed + 1000)
@@ -138,6 +142,8 @@ def make_prefill(spec: PrefillSpec, device="cpu", *, n: int | None = None) -> di
         for bb in range(B):
             a_idx = _ar1_drift(n, d, rng)
             k_idx[bb] = (k_idx[bb].float() + torch.from_numpy(a_idx).float().to(device)).to(torch.bfloat16)
+            if indexer_only:
+                continue
             for g in range(spec.hkv):
                 a_k = _ar1_drift(n, d, rng)
                 k[bb, g] = (k[bb, g].float() + torch.from_numpy(a_k).float().to(device)).to(torch.bfloat16)

@@ -60,8 +60,10 @@ typedef enum {
 
 /*
  * Method parameters.  Fields the pages fix: n_idx_heads = 4, head_dim = 128,
- * rope_dims = 64, r and k_tokens (K) [KI].  Fields the pages leave open and this
- * library states explicitly:
+ * rope_dims = 64, r and k_tokens (K) [KI]; the paperglide reader's Fig. 5(b)
+ * varies the number of indexer query heads and Fig. 5(a) / 6(a,b) the
+ * micro-block size r, so both are runtime parameters here.  Fields the pages
+ * leave open and this library states explicitly:
  *   rope_base  -- RoPE base (10000 in every workload here).
  *   rmsnorm    -- 1 = unit-weight RMSNorm between pooling and RoPE (the [QSA]
  *                 toy mentions it, [KI] does not); 0 = off (default).
@@ -72,7 +74,7 @@ typedef enum {
  */
 typedef struct {
   int32_t r;            /* tokens per micro-block (1..16, power of two) */
-  int32_t n_idx_heads;  /* indexer query heads; must be 4 */
+  int32_t n_idx_heads;  /* indexer query heads: 1, 2, 4 or 8 (4 in [KI]) */
   int32_t head_dim;     /* must be 128 */
   int32_t rope_dims;    /* rotated dims, even, <= head_dim (64) */
   float rope_base;      /* > 0 */
@@ -82,7 +84,9 @@ typedef struct {
 } qsa_config;
 
 /* Fills `cfg` with the configuration of [KI]: r = 4, 4 indexer heads, d = 128,
- * 64 rotated dims, base 10000, no RMSNorm, K = 2048. */
+ * 64 rotated dims, base 10000, no RMSNorm, K = 2048.  An n_idx_heads outside
+ * {1, 2, 4, 8} or a head_dim other than 128 makes every call return
+ * QSA_ERR_UNSUPPORTED. */
 void qsa_default_config(qsa_config* cfg);
 
 /* k_B = ceil(K / r) for `cfg` (0 on a null or invalid cfg). */
@@ -115,11 +119,11 @@ size_t qsa_index_topk_workspace(const qsa_config* cfg, int64_t B, int64_t n_q,
 
 /*
  * Indexer scoring and top-k_B block selection [KI], [QSA] steps 3-4:
- *   I_ib = sum_{h < 4} ReLU(<qt_i^h, kbar_b>)   for b < c_i,
+ *   I_ib = sum_{h < H} ReLU(<qt_i^h, kbar_b>)   for b < c_i,  H = n_idx_heads,
  * where qt_i^h = bf16(RoPE_{floor(i/r)}(q_idx[i, h])).  For each row, if
  * c_i <= k_B every visible block is kept; otherwise the k_B blocks with the
  * largest I_ib, an equal score going to the lower block id.
- *   q_idx   bf16 [B][n_q][4][head_dim], un-rotated indexer queries.
+ *   q_idx   bf16 [B][n_q][H][head_dim], un-rotated indexer queries.
  *   kbar    bf16 compressed keys as written by qsa_compress_keys; sequence bb
  *           at kbar + bb * kbar_stride_b elements, holding >= c_i rows for its
  *           last query row.

@@ -65,7 +65,7 @@ def _cfg(**kw):
 @pytest.mark.parametrize("field,value,status", [
     ("r", 3, 1), ("r", 0, 1), ("r", 32, 1), ("rope_dims", 63, 1), ("rope_dims", 130, 1),
     ("rope_base", -1.0, 1), ("k_tokens", 0, 1), ("rmsnorm", 2, 1),
-    ("head_dim", 64, 2), ("n_idx_heads", 2, 2),
+    ("head_dim", 64, 2), ("n_idx_heads", 3, 2), ("n_idx_heads", 16, 2), ("n_idx_heads", 0, 2),
 ])
 def test_invalid_config_rejected_before_launch(lib, field, value, status):
     c = _cfg()
@@ -132,3 +132,13 @@ def test_fallback_rows_checks_before_any_cuda_call(lib):
     assert lib.qsa_index_topk_fallback_rows(ctypes.byref(c), 1, 4, 512, fake, ws_scan,
                                             ctypes.byref(rows), None) == 0
     assert rows.value == 0
+
+
+@pytest.mark.parametrize("h", [1, 2, 4, 8])
+def test_indexer_head_counts_are_accepted(lib, h):
+    """1, 2, 4 or 8 indexer query heads: the workspace grows with the rotated
+    queries (n_q x h x 128 bf16) and nothing is refused on the host."""
+    c = _cfg(n_idx_heads=h)
+    ws = lib.qsa_index_topk_workspace(ctypes.byref(c), 1, 2048, 512)
+    assert ws >= 2048 * h * 128 * 2
+    assert lib.qsa_index_topk_workspace(ctypes.byref(c), 1, 3, 512) >= 3 * h * 128 * 2

@@ -21,7 +21,8 @@ DEV = "cuda"
 
 
 def cfg_for(spec, **kw) -> qsa.Config:
-    base = dict(r=spec.r, rope_dims=spec.rope_dims, rope_base=spec.rope_base, k_tokens=spec.k_tokens)
+    base = dict(r=spec.r, rope_dims=spec.rope_dims, rope_base=spec.rope_base, k_tokens=spec.k_tokens,
+                n_idx_heads=spec.h_idx)
     base.update(kw)
     return qsa.Config(**base)
 
@@ -312,6 +313,58 @@ def test_batched_prefill_sequences_at_different_offsets():
                                 lse[b].cpu().numpy(), cfg.k_b, cfg.r, attn=(qb, kb, vb))
         exact += st["exact"]
     assert exact >= 3 * len(rows) - 1
+
+
+# ----------------------------------------------------------------------------- indexer head counts
+
+@pytest.mark.parametrize("h_idx", [1, 2, 8])
+def test_indexer_head_counts_prefill_fused_path(h_idx):
+    """H indexer query heads through the fused tcgen05 indexer (n_q >= 64 rows,
+    k_B <= 512): tiles of 48 tokens (24 with 8 heads), N = tokens x H."""
+    spec = PrefillSpec("h", n=3000, k_tokens=512, seed=60 + h_idx, h_idx=h_idx)
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    gpu = run_prefill(cfg, wl)
+    rows = list(range(0, 3000, 7)) + list(range(2040, 2060)) + [2999]
+    res = QC.oracle_rows(wl, rows, cfg=cfg)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, cfg.r)
+    assert st["exact"] >= 0.98 * len(rows), st
+
+
+@pytest.mark.parametrize("h_idx", [1, 2, 8])
+def test_indexer_head_counts_scan_path(h_idx):
+    """A 40-row chunk (fewer than 64 rows: the one-pass scan path, 8 / H rows per
+    MMA tile) at offset 1500, and r = 2 rows of a whole prefill (k_B = 1024 >
+    512: the scan path too)."""
+    spec = PrefillSpec("h", n=2600, k_tokens=512, seed=70 + h_idx, h_idx=h_idx)
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    lo, hi = 1500, 1540
+    gpu = run_prefill(cfg, wl, q_pos0=lo, rows=slice(lo, hi))
+    res = QC.oracle_rows({**wl, "q_idx": wl["q_idx"][:, lo:hi], "q": wl["q"][:, lo:hi]}, range(hi - lo), cfg=cfg,
+                         q_pos0=lo)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, cfg.r)
+    assert st["exact"] >= hi - lo - 1, st
+    spec2 = PrefillSpec("h2", n=2600, k_tokens=2048, seed=80 + h_idx, h_idx=h_idx, r=2)
+    wl2 = make_prefill(spec2, DEV)
+    cfg2 = cfg_for(spec2)
+    gpu2 = run_prefill(cfg2, wl2)
+    rows = [0, 1, 2047, 2048, 2049, 2050, 2599] + list(range(100, 2600, 97))
+    res2 = QC.oracle_rows(wl2, rows, cfg=cfg2)
+    st2 = QC.compare_prefill(res2, gpu2["idx"][0], gpu2["count"][0], gpu2["out"][0], gpu2["lse"][0], cfg2.k_b, cfg2.r)
+    assert st2["exact"] >= len(rows) - 1, st2
+
+
+@pytest.mark.parametrize("h_idx,next_n", [(1, 1), (2, 3), (8, 1), (8, 3), (1, 4)])
+def test_indexer_head_counts_decode(h_idx, next_n):
+    """Decode with H indexer heads: the k-bar scan puts 8 / H query rows in each
+    MMA tile (one new token, or next_n tokens scored in one pass)."""
+    spec = DecodeSpec("dh", batch=3, ctx=5003, k_tokens=512, seed=90 + h_idx, next_n=next_n, h_idx=h_idx)
+    wl = make_decode(spec, DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode_multi(cfg, wl)
+    exact = sum(check_decode_multi_seq(cfg, wl, bb, idx, cnt, out, lse)["exact"] for bb in range(3))
+    assert exact >= 3 * next_n - 1
 
 
 def test_rmsnorm_variant_end_to_end():
