@@ -22,8 +22,9 @@
 //   1. Pilot: a strided sample of the tile's blocks (every 16th block, in one
 //      or more phases) is scored first and binned per token into 512 bins of
 //      1/16 octave of the fp32 score (16-bit counters, two per word).  From it
-//      each token takes a threshold tau above which about 1.6 k_B of its scores
-//      are expected (interpolated inside the bin where the count is reached).
+//      each token takes a threshold tau above which about sqrt(k_B kFCap) of
+//      its scores are expected (interpolated inside the bin where the count is
+//      reached).
 //   2. Collect: every chunk is scored; each (token, block) with score >= tau is
 //      appended (bit pattern u of 2 x score, block id) to the token's buffer in
 //      global memory: one segment per TMEM lane quarter, so that no two warps
@@ -45,6 +46,8 @@
 // flag, every role leaves its loop, in-flight copies and MMAs are waited for
 // (bounded), TMEM is freed and the device error word reports the timeout.
 #include <cudaTypedefs.h>
+
+#include <cmath>
 
 #include "common.cuh"
 #include "sm100.cuh"
@@ -117,8 +120,15 @@ struct TileMeta {
 
 constexpr int kPilotStride = 16;   // the pilot samples every 16th block (per phase)
 constexpr int kPilotMin = 2048;    // at least this many pilot samples per row when possible
-constexpr int kPilotNum = 8;       // tau aims at kPilotNum / kPilotDen x k_B entries per row:
-constexpr int kPilotDen = 5;       // near the middle, in ratio, of the accepted [k_B, 2.5 k_B]
+// tau aims at sqrt(k_B kFCap) entries per row, the middle in ratio of the
+// accepted [k_B, kFCap]: 1.6 k_B at k_B = 512, 3.2 k_B at k_B = 128, where the
+// quantile sought lies further in the tail and the pilot's estimate of it is
+// noisier
+// (never below 1.6 k_B).
+inline int pilot_aim(int k_b) {
+  const double g = std::sqrt((double)k_b * kFCap), lo = 1.6 * k_b;
+  return (int)((g > lo ? g : lo) + 0.5);
+}
 
 template <int TT>
 __device__ __forceinline__ TileMeta tile_meta(int64_t t, int64_t tiles_per_seq, int64_t n_q,
@@ -332,7 +342,7 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
 
 // ---------------------------------------------------------------------------------------------
 // Threshold of one token from its pilot histogram (one warp).  want =
-// ceil(kPilotNum k_B P / (kPilotDen c)) of the P samples should lie at or above
+// ceil(aim P / c) of the P samples should lie at or above
 // tau: the bin where the count from the top reaches want is found, and tau is
 // placed inside it by linear interpolation, as if its samples were spread
 // evenly over its value range (the bins are 1/16 octave wide, and in the far
@@ -340,7 +350,7 @@ __device__ __forceinline__ void finalize_row(const uint2* __restrict__ seg, int 
 // it).  tau is 0 when the bottom bin is reached or the row has no samples,
 // which collects every visible block.  The histogram is cleared for the next
 // tile.  Lane L owns bins 16 (31 - L) .. + 15.
-__device__ __forceinline__ uint32_t pilot_tau(uint32_t* __restrict__ hist, int64_t c, int k_b) {
+__device__ __forceinline__ uint32_t pilot_tau(uint32_t* __restrict__ hist, int64_t c, int aim) {
   const int lane = threadIdx.x & 31;
   uint4* const w4 = reinterpret_cast<uint4*>(hist + 8 * (31 - lane));
   const uint4 lo4 = w4[0], hi4 = w4[1];
@@ -361,7 +371,7 @@ __device__ __forceinline__ uint32_t pilot_tau(uint32_t* __restrict__ hist, int64
     if (lane >= o) incl += y;
   }
   const int64_t P = __shfl_sync(0xffffffffu, incl, 31);
-  int64_t want = (kPilotNum * (int64_t)k_b * P + kPilotDen * c - 1) / (kPilotDen * c);
+  int64_t want = ((int64_t)aim * P + c - 1) / c;
   if (want < 1) want = 1;
   const int above0 = incl - sum;
   const bool cross = above0 < want && incl >= want;
@@ -408,7 +418,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
 index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_kp, const int64_t* __restrict__ q_pos,
                         int64_t n_q, int64_t tiles_per_seq, int64_t t_begin, int64_t t_count, int rshift,
-                        int k_b, int64_t c_cap, uint2* __restrict__ buf, int* __restrict__ cnt) {
+                        int k_b, int aim, int64_t c_cap, uint2* __restrict__ buf, int* __restrict__ cnt) {
   using namespace sm100;
   using Sh = FusedShape<H>;
   constexpr int TT = Sh::TT, TPW = Sh::TPW, CPW = Sh::CPW;
@@ -571,7 +581,7 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           for (int t = ew; t < TT; t += kEpiWarps) {
             const int64_t c = token_c(m, t, rshift, c_cap);
             // Rows that do not select (past the end, or c <= k_B) collect nothing.
-            const uint32_t tau = pilot_tau(S.phist[t], c, k_b);
+            const uint32_t tau = pilot_tau(S.phist[t], c, aim);
             if (lane == 0) S.tau[t] = (t < m.nvalid && c > k_b) ? tau : 0xffffffffu;
           }
           __syncwarp();
@@ -856,7 +866,7 @@ struct FusedLayout {
 };
 
 // Workspace of the fused path (after the rotated queries): the entry buffers of
-// one launch's tiles (48 tokens x 4 segments x kSeg entries per tile) and their
+// one launch's tiles (48 or 24 tokens x 4 segments x kSeg entries per tile) and their
 // counts, the fallback row list and counter, and the fallback kernel's score rows.
 inline FusedLayout fused_layout(int64_t B, int64_t n_q, int64_t n_blocks_max, int H) {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -898,6 +908,7 @@ cudaError_t launch_index_fused(int H, const __nv_bfloat16* qt, const __nv_bfloat
   if (H != 1 && H != 2 && H != 4 && H != 8) return cudaErrorInvalidValue;
   const FusedLayout L = fused_layout(B, n_q, n_blocks_max, H);
   const int tt = fused_tile_tokens(H);
+  const int aim = pilot_aim(k_b);
   if (L.n_tiles == 0) return cudaSuccess;
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
@@ -970,7 +981,7 @@ cudaError_t launch_index_fused(int H, const __nv_bfloat16* qt, const __nv_bfloat
     if (grid > t_count) grid = t_count;
 #define QSA_FUSED_LAUNCH(HH)                                                                                 \
   index_topk_fused_kernel<HH><<<(unsigned)grid, kFThreads, kFusedSmemBytes, st>>>(                           \
-      tm_q, tm_k, tm_kp, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, n_blocks_max, buf, cnt)
+      tm_q, tm_k, tm_kp, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, aim, n_blocks_max, buf, cnt)
     switch (H) {
       case 1: QSA_FUSED_LAUNCH(1); break;
       case 2: QSA_FUSED_LAUNCH(2); break;

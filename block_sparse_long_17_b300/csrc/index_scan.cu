@@ -193,6 +193,7 @@ decode_scan_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16* __
                    int64_t c_cap, int64_t tiles_per_seq, int64_t tiles_per_warp, float* __restrict__ S,
                    int64_t s_stride) {
   constexpr int R = 8 / H;
+  griddep_wait();  // the rotated queries come from the previous kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, t = lane & 3;
   const int64_t wid = (int64_t)blockIdx.x * kScanWarps + warp;
@@ -291,10 +292,9 @@ static cudaError_t launch_decode_scan_nt(const __nv_bfloat16* qt, const __nv_bfl
   const int64_t tiles_per_warp = (total + warps - 1) / warps;
   warps = (total + tiles_per_warp - 1) / tiles_per_warp;
   const int64_t grid = (warps + kScanWarps - 1) / kScanWarps;
-  decode_scan_kernel<H, NT><<<(unsigned)grid, kScanWarps * 32, 0, st>>>(qt, kbar, kbar_stride_b, q_pos, B, n_q, r,
-                                                                        c_max, tiles_per_seq, tiles_per_warp, S,
-                                                                        s_stride);
-  return count_launch(cudaGetLastError());
+  return count_launch(launch_dependent(decode_scan_kernel<H, NT>, dim3((unsigned)grid), dim3(kScanWarps * 32), 0, st,
+                                      qt, kbar, kbar_stride_b, q_pos, B, n_q, r, c_max, tiles_per_seq,
+                                      tiles_per_warp, S, s_stride));
 }
 
 // Scores of the n_q <= kDecodeMaxRows query rows of each sequence in one pass

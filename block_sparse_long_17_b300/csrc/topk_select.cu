@@ -306,8 +306,8 @@ __device__ void select_from_candidates(SelectFastSmem& sm, int ncand, uint32_t l
 }
 
 // ---------------------------------------------------------------------------------------------
-// The same selection with each row split over a cluster of kSelCluster = 4
-// CTAs (decode: few rows, long rows).  Every CTA takes a quarter of the row: local
+// The same selection with each row split over a cluster of kSelCluster CTAs
+// (decode: few rows, long rows).  Every CTA takes a share of the row: local
 // histograms of the top 11 bits, merged by every CTA through distributed
 // shared memory; ordered copies of the entries at or above the boundary bin,
 // gathered into the first CTA's candidate arrays in rank (= block) order; that
@@ -320,6 +320,7 @@ topk_select_cluster_kernel(const float* __restrict__ S, int64_t s_stride, const 
   namespace cg = cooperative_groups;
   __shared__ SelectFastSmem sm;
   __shared__ int n_local;
+  griddep_wait();  // the scores come from the previous kernel
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int64_t lrow = blockIdx.x / kSelCluster;
@@ -455,13 +456,16 @@ topk_select_cluster_kernel(const float* __restrict__ S, int64_t s_stride, const 
   if (threadIdx.x == 0) count[row] = k_b;
 }
 
+// Clusters of 4 CTAs per row.  (Clusters of 8 were slower at 16 rows of
+// 262144 scores: the cluster barriers and the first CTA's refinement, not the
+// passes over the row, set the time.)
 cudaError_t launch_topk_select_cluster(const float* S, int64_t s_stride, const int64_t* q_pos, int64_t n_q,
                                        int64_t row_lo, int64_t n_rows, int r, int k_b, int64_t c_cap,
                                        int32_t* idx, int32_t* count, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
-  topk_select_cluster_kernel<4><<<(unsigned)(n_rows * 4), kSelThreads, 0, st>>>(S, s_stride, q_pos, n_q, row_lo,
-                                                                                r, k_b, c_cap, idx, count);
-  return count_launch(cudaGetLastError());
+  return count_launch(launch_dependent(topk_select_cluster_kernel<4>, dim3((unsigned)(n_rows * 4)),
+                                       dim3(kSelThreads), 0, st, S, s_stride, q_pos, n_q, row_lo, r, k_b, c_cap, idx,
+                                       count));
 }
 
 
