@@ -58,6 +58,10 @@ inline cudaError_t ensure_dyn_smem(const void* kernel, int bytes) {
   std::lock_guard<std::mutex> lock(mu);
   if (done.count({kernel, dev})) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  // All of the unified L1/shared storage as shared memory, so that the
+  // occupancy the kernel was sized for (for some kernels two CTAs per SM) is
+  // available.
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e == cudaSuccess) done.insert({kernel, dev});
   return e;
 }

@@ -88,6 +88,7 @@ rotate_queries_kernel(const __nv_bfloat16* __restrict__ q_idx, const int64_t* __
                       __nv_bfloat16* __restrict__ qt) {
   __shared__ float cs[kCompressWarps][2][kMaxRopePairs];
   __shared__ float row[kCompressWarps][kHeadDim];
+  griddep_wait();  // launched dependent: the previous kernel may still write its inputs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t item = (int64_t)blockIdx.x * kCompressWarps + warp;
   if (item >= B * n_q) return;
@@ -140,9 +141,8 @@ cudaError_t launch_rotate_queries(const __nv_bfloat16* q_idx, const int64_t* q_p
   const int64_t items = B * n_q;
   if (items == 0) return cudaSuccess;
   const int64_t grid = (items + kCompressWarps - 1) / kCompressWarps;
-  rotate_queries_kernel<<<(unsigned)grid, kCompressWarps * 32, 0, st>>>(q_idx, q_pos, B, n_q, r, n_heads,
-                                                                         rope, qt);
-  return count_launch(cudaGetLastError());
+  return count_launch(launch_dependent(rotate_queries_kernel, dim3((unsigned)grid), dim3(kCompressWarps * 32), 0, st,
+                                      q_idx, q_pos, B, n_q, r, n_heads, rope, qt));
 }
 
 }  // namespace qsa

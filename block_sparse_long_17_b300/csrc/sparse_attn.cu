@@ -357,6 +357,7 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
                           float* __restrict__ part_ml, int* __restrict__ unit_done,
                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   extern __shared__ __align__(128) uint8_t attn_smem[];
+  griddep_wait();  // the selection and the zeroed counters come from the previous kernels
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
   uint8_t* const wbuf = attn_smem + warp * kAWarpBytes;
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(wbuf));
@@ -423,6 +424,14 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
   }
 }
 
+// Zeroes the completion counters of a decode call (launched dependent, so it
+// waits for the previous kernel, which may be the last call's attention still
+// using them).
+__global__ void zero_counters_kernel(int* __restrict__ p, int64_t n) {
+  griddep_wait();
+  for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += (int64_t)gridDim.x * blockDim.x) p[j] = 0;
+}
+
 // Most splits a (sequence, kv head, head chunk) can use: splits of at least
 // kDecodeMinSplit slots over the longest token set, k_b r + r - 1.
 int decode_max_splits(int k_b, int r) {
@@ -482,7 +491,9 @@ cudaError_t launch_sparse_attn_decode(const __nv_bfloat16* q, const __nv_bfloat1
   float* part_ml = part_o + units * max_split * 8 * kHeadDim;
   const size_t parts = (size_t)units * max_split * (8 * kHeadDim + 16) * sizeof(float);
   int* unit_done = reinterpret_cast<int*>(static_cast<char*>(ws) + (parts + 255) / 256 * 256);
-  cudaError_t e = cudaMemsetAsync(unit_done, 0, (size_t)units * sizeof(int), st);
+  const int64_t zblocks = (units + 255) / 256;
+  cudaError_t e = count_launch(launch_dependent(zero_counters_kernel, dim3((unsigned)(zblocks < 1024 ? zblocks : 1024)),
+                                                dim3(256), 0, st, unit_done, units));
   if (e != cudaSuccess) return e;
   // As many splits per unit as fill the resident warps once (at least one,
   // at most max_split), each a whole number of 16-slot groups.
@@ -500,10 +511,9 @@ cudaError_t launch_sparse_attn_decode(const __nv_bfloat16* q, const __nv_bfloat1
   n_split = (max_tok + split_len - 1) / split_len;
   e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), units * n_split, &grid);
   if (e != cudaSuccess) return e;
-  sparse_attn_decode_kernel<<<grid, kAWarps * 32, kASmemBytes, st>>>(
-      q, k, v, L_cap, cache_len, idx, count, B, n_q, Hq, Hkv, r, k_b, (int)n_split, split_len, scale, part_o, part_ml,
-      unit_done, out, lse);
-  return count_launch(cudaGetLastError());
+  return count_launch(launch_dependent(sparse_attn_decode_kernel, dim3((unsigned)grid), dim3(kAWarps * 32),
+                                      (size_t)kASmemBytes, st, q, k, v, L_cap, cache_len, idx, count, B, n_q, Hq, Hkv,
+                                      r, k_b, (int)n_split, split_len, scale, part_o, part_ml, unit_done, out, lse));
 }
 
 }  // namespace qsa

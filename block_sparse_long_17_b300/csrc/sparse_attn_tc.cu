@@ -34,13 +34,17 @@
 //   O is kept in registers: each stage's PV lands in a fresh TMEM buffer and is
 //   folded in with that stage's rescale factor.
 //
-// Warp roles (288 threads, two CTAs per SM): warps 0-3 issue the TMA loads
-// (a TMA copy takes its issuing warp about a hundred cycles, so a single
-// issuing warp caps the gather rate; four of them each issue a quarter of
-// every stage's slots), warp 4 the MMAs, warps 5-8 read TMEM (one 32-lane
-// quarter each) and run the softmax.  Every wait is bounded; on a timeout the CTA raises its abort flag,
-// the roles drain without further work, in-flight copies and MMAs are waited
-// for and TMEM is freed, and the device error word reports the timeout.
+// Warp roles (256 threads, two CTAs per SM).  Warps 0-2 issue the TMA loads:
+// a TMA copy takes its issuing warp about a hundred cycles, so one issuing
+// warp caps the gather rate, and each of the three issues a third of every
+// stage's slots.  K of a stage is loaded as soon as its ring slot frees after
+// that stage's scores MMA, V one stage later, as its slot frees only after
+// the PV MMA.  Warp 3 issues the MMAs; warps 4-7 read TMEM (one 32-lane
+// quarter each) and run the softmax.  Two CTAs of 8 warps at up to 128
+// registers fit an SM (each of its four schedulers holds 16K registers).
+// Every wait is bounded; on a timeout the CTA raises its abort flag, the
+// roles drain without further work, in-flight copies and MMAs are waited for
+// and TMEM is freed, and the device error word reports the timeout.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -49,10 +53,10 @@
 namespace qsa {
 
 constexpr int kTcStages = 3;                         // K/V ring depth
-constexpr int kTcProducers = 4;                      // TMA-issuing warps (each a quarter of a stage's slots)
+constexpr int kTcProducers = 3;                      // TMA-issuing warps (each a third of a stage's slots)
 constexpr int kTcEpiWarps = 4;
-constexpr int kTcMmaWarp = kTcProducers;             // warp 4
-constexpr int kTcThreads = 32 * (kTcProducers + 1 + kTcEpiWarps);  // 288
+constexpr int kTcMmaWarp = kTcProducers;             // warp 3
+constexpr int kTcThreads = 32 * (kTcProducers + 1 + kTcEpiWarps);  // 256
 constexpr int kTcStageBytes = 128 * 128;             // 128 rows of 128 B: 64 tokens
 constexpr int kTcGroup = 8;                          // query heads per kv head
 constexpr uint32_t kTcTmemCols = 64;                 // S: 2 x 16 columns, O: 2 x 16 columns
@@ -66,7 +70,7 @@ struct TcSmem {
   uint8_t p[2][4096];   // P' of two stages: 16 rows x 128 stage rows, two 64-row slabs
   float red[2][kTcEpiWarps][8];
   float lred[kTcEpiWarps][8];
-  uint64_t k_full[kTcStages], v_full[kTcStages], kv_empty[kTcStages];
+  uint64_t k_full[kTcStages], v_full[kTcStages], k_empty[kTcStages], v_empty[kTcStages];
   uint64_t q_full[2], q_empty[2], s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -122,18 +126,21 @@ __device__ __forceinline__ int tc_loaded_slots(const TcUnit& U, int s, int sps, 
   return n < sps ? n : sps;
 }
 
-// First token of slot `slot`'s box: a selected block, or the box ending at i
-// (the tail, and any padding slot).
-__device__ __forceinline__ int tc_slot_start(const TcUnit& U, const int32_t* __restrict__ sel, int slot, int r) {
-  if (slot < U.cnt) {
-    int64_t b = __ldg(sel + slot);
-    if ((uint64_t)b >= (uint64_t)U.c) {  // malformed selection: read block 0, report
-      flag_device_error(kDevErrBlockId);
-      b = 0;
-    }
-    return (int)(b * r);
+// Slot `slot`'s selected block id, or -1 for the tail (and any padding slot):
+// a plain load, so that it can be issued a stage before its use.
+__device__ __forceinline__ int tc_slot_block(const TcUnit& U, const int32_t* __restrict__ sel, int slot) {
+  return slot < U.cnt ? __ldg(sel + slot) : -1;
+}
+
+// First token of a slot's box: block b's first token, or for b = -1 the box
+// ending at i (the tail, and any padding slot).
+__device__ __forceinline__ int tc_slot_start(const TcUnit& U, int b, int r) {
+  if (b < 0) return (int)(U.i - r + 1);
+  if ((int64_t)b >= U.c) {  // malformed selection: read block 0, report
+    flag_device_error(kDevErrBlockId);
+    b = 0;
   }
-  return (int)(U.i - r + 1);
+  return b * r;
 }
 
 // Bounded wait by every lane of a warp.  After a timeout (abort flag raised)
@@ -167,8 +174,7 @@ __device__ __forceinline__ void st_global_cs_b16(__nv_bfloat16* p, float x) {
   asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p), "h"(*reinterpret_cast<const unsigned short*>(&h)) : "memory");
 }
 
-// Two CTAs per SM: 65536 registers over 2 x 288 threads.
-__global__ void __maxnreg__(112)
+__global__ void __launch_bounds__(kTcThreads, 2)
 sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, int64_t L_cap, const int64_t* __restrict__ q_pos,
                       const int32_t* __restrict__ idx, const int32_t* __restrict__ count, int64_t B, int64_t n_q,
@@ -190,7 +196,8 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&S.k_full[s], kTcProducers);
       mbar_init(&S.v_full[s], kTcProducers);
-      mbar_init(&S.kv_empty[s], 1);
+      mbar_init(&S.k_empty[s], 1);
+      mbar_init(&S.v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.q_full[b], 1);
@@ -223,10 +230,26 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   if (warp < kTcProducers) {
     // ------------------------------------------------------------ TMA producers
     const uint64_t pol_stream = policy_evict_first();
-    const int qs = sps / kTcProducers;  // slots of each producer per stage
-    const int my0 = warp * qs;
-    uint32_t gst = 0, gu = 0;
+    // This warp's slots of every stage: [my0, my1).
+    const int my0 = warp * sps / kTcProducers, my1 = (warp + 1) * sps / kTcProducers;
+    const int qs = my1 - my0;
+    uint32_t gst = 0, gu = 0, v_issued = 0;
     bool ok = true;
+    // V of global stage g: this warp's `mine` slots, lane l's box at token
+    // `ts` of head `head` (the same boxes as that stage's K).
+    int pv_mine = 0, pv_ts = 0, pv_head = 0;
+    auto issue_v = [&](uint32_t g, int mine, int ts, int head) -> bool {
+      const int st = (int)(g % kTcStages);
+      bool w = true;
+      if (lane == 0) w = mbar_wait(&S.v_empty[st], ((g / kTcStages) & 1) ^ 1, abort_flag, kWaitCycles, 64);
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) return false;
+      if (lane == 0) mbar_arrive_expect_tx(&S.v_full[st], (uint32_t)(mine * box));
+      __syncwarp();
+      if (lane < mine) tma_load_4d(S.v[st] + (my0 + lane) * box, &tm_v, &S.v_full[st], 0, 0, ts, head);
+      v_issued = g + 1;
+      return true;
+    };
     for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
       const TcUnit U = tc_unit(u, rows, n_q, Hkv, q_pos, count, L_cap, r, k_b, sps, false);
       if (U.skip || U.n_stages == 0) continue;
@@ -244,33 +267,37 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (!ok) break;
       ++gu;
       const int32_t* sel = idx + U.row * (int64_t)k_b;
+      // Block ids are loaded one stage ahead of their use.
+      int blk = lane < qs ? tc_slot_block(U, sel, my0 + lane) : -1;
       for (int s = 0; s < U.n_stages; ++s, ++gst) {
+        const int blk_next = (lane < qs && s + 1 < U.n_stages) ? tc_slot_block(U, sel, (s + 1) * sps + my0 + lane) : -1;
+        // K of this stage (its slot frees as soon as the scores MMA is done) ...
         const int st = (int)(gst % kTcStages);
-        if (lane == 0) ok = mbar_wait(&S.kv_empty[st], ((gst / kTcStages) & 1) ^ 1, abort_flag, kWaitCycles, 64);
+        if (lane == 0) ok = mbar_wait(&S.k_empty[st], ((gst / kTcStages) & 1) ^ 1, abort_flag, kWaitCycles, 64);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const int n_ld = tc_loaded_slots(U, s, sps, spk);
         int mine = n_ld - my0;  // this warp's loaded slots: [my0, my0 + mine)
         mine = mine < 0 ? 0 : (mine > qs ? qs : mine);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&S.k_full[st], (uint32_t)(mine * box));
-          mbar_arrive_expect_tx(&S.v_full[st], (uint32_t)(mine * box));
-        }
+        if (lane == 0) mbar_arrive_expect_tx(&S.k_full[st], (uint32_t)(mine * box));
         __syncwarp();
-        if (lane < mine) {
-          const int sl = my0 + lane;
-          const int ts = tc_slot_start(U, sel, s * sps + sl, r);
-          tma_load_4d(S.k[st] + sl * box, &tm_k, &S.k_full[st], 0, 0, ts, U.head);
-          tma_load_4d(S.v[st] + sl * box, &tm_v, &S.v_full[st], 0, 0, ts, U.head);
-        }
+        const int ts = lane < mine ? tc_slot_start(U, blk, r) : 0;
+        blk = blk_next;
+        if (lane < mine) tma_load_4d(S.k[st] + (my0 + lane) * box, &tm_k, &S.k_full[st], 0, 0, ts, U.head);
+        // ... then V of the previous stage, whose slot frees only after its PV.
+        if (gst > 0 && !issue_v(gst - 1, pv_mine, pv_ts, pv_head)) { ok = false; break; }
+        pv_mine = mine;
+        pv_ts = ts;
+        pv_head = U.head;
       }
     }
+    if (ok && gst > 0) ok = issue_v(gst - 1, pv_mine, pv_ts, pv_head);
     if (!ok && lane == 0) {
       volatile int never = 0;  // wait (bounded) for copies still in flight
-      for (uint32_t j = (gst > kTcStages ? gst - kTcStages : 0); j < gst; ++j) {
+      for (uint32_t j = (gst > kTcStages ? gst - kTcStages : 0); j < gst; ++j)
         mbar_wait(&S.k_full[j % kTcStages], (j / kTcStages) & 1, &never, 100000000LL);
+      for (uint32_t j = (v_issued > kTcStages ? v_issued - kTcStages : 0); j < v_issued; ++j)
         mbar_wait(&S.v_full[j % kTcStages], (j / kTcStages) & 1, &never, 100000000LL);
-      }
       if (warp == 0 && gu > 0) mbar_wait(&S.q_full[(gu - 1) & 1], ((gu - 1) >> 1) & 1, &never, 100000000LL);
     }
   } else if (warp == kTcMmaWarp) {
@@ -296,7 +323,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           umma_bf16(d, desc_mnmajor_sw128(a0 + (uint32_t)kk * 2048),
                     desc_kmajor_sw128(b0 + (uint32_t)(kk >> 2) * 2048 + (uint32_t)(kk & 3) * 32), idesc_pv,
                     kk > 0 ? 1u : 0u);
-        umma_commit(&S.kv_empty[st]);
+        umma_commit(&S.v_empty[st]);
         umma_commit(&S.p_empty[b2]);
         umma_commit(&S.o_full[b2]);
         return true;
@@ -319,6 +346,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(tmem + b2 * 16, desc_kmajor_sw128(ka + kk * 32), desc_kmajor_sw128(qa + kk * 32), idesc_s,
                       kk > 0 ? 1u : 0u);
+          umma_commit(&S.k_empty[st]);
           umma_commit(&S.s_full[b2]);
           if (s == U.n_stages - 1) umma_commit(&S.q_empty[qb]);
           // The previous stage's PV goes after this stage's scores, so that the
@@ -539,13 +567,13 @@ cudaError_t launch_sparse_attn_tc(const __nv_bfloat16* q, const __nv_bfloat16* k
   }
   cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(sparse_attn_tc_kernel), (int)kTcSmemBytes);
   if (e != cudaSuccess) return e;
-  int sms = 0, per_sm = 0;
+  // Two CTAs per SM: registers (8 warps x 128) and shared memory (2 x 113 KB of
+  // 228 KB) both allow it.  The kernel is persistent with no dependence between
+  // CTAs, so the result does not depend on how many are resident at once.
+  int sms = 0;
   e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sparse_attn_tc_kernel, kTcThreads, kTcSmemBytes);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  int64_t grid = (int64_t)sms * per_sm;
+  int64_t grid = (int64_t)sms * 2;
   if (grid > units) grid = units;
   sparse_attn_tc_kernel<<<(unsigned)grid, kTcThreads, kTcSmemBytes, st>>>(
       tm_q, tm_k, tm_v, L_cap, q_pos, idx, count, B, n_q, Hq, Hkv, r, k_b, scale * 1.4426950408889634f, out, lse);
