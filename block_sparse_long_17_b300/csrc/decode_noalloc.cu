@@ -63,7 +63,7 @@ bool on_current_device(int dev, const void* q, cudaStream_t st) {
     cudaGetLastError();
     return false;
   }
-  return at.type == cudaMemoryTypeDevice && at.device == dev;
+  return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
 }
 
 }  // namespace

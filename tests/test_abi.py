@@ -142,3 +142,23 @@ def test_indexer_head_counts_are_accepted(lib, h):
     ws = lib.qsa_index_topk_workspace(ctypes.byref(c), 1, 2048, 512)
     assert ws >= 2048 * h * 128 * 2
     assert lib.qsa_index_topk_workspace(ctypes.byref(c), 1, 3, 512) >= 3 * h * 128 * 2
+
+
+def test_attention_kernel_choice_checked_on_the_host(lib):
+    """qsa_sparse_attn_prefill_impl: a kernel choice outside the enum is an
+    invalid argument and the tcgen05 kernel's shape limits are checked before
+    any launch (no device pointer is touched)."""
+    c = _cfg()
+    fake = ctypes.c_void_p(256)
+    args = (ctypes.byref(c), fake, fake, fake, 8, fake, fake, fake, 1, 4, 16, 2, 0.0, fake, None)
+    assert lib.qsa_sparse_attn_prefill_impl(*args, 7, None) == 1
+    assert lib.qsa_sparse_attn_prefill_impl(*args, -1, None) == 1
+    c12 = _cfg()
+    bad = (ctypes.byref(c12), fake, fake, fake, 8, fake, fake, fake, 1, 4, 12, 4, 0.0, fake, None)
+    assert lib.qsa_sparse_attn_prefill_impl(*bad, 1, None) == 2   # tcgen05: 3 query heads per kv head
+    c2 = _cfg(r=2)
+    r2 = (ctypes.byref(c2), fake, fake, fake, 8, fake, fake, fake, 1, 4, 16, 2, 0.0, fake, None)
+    assert lib.qsa_sparse_attn_prefill_impl(*r2, 1, None) == 2     # tcgen05: r = 2
+    # empty work succeeds without a launch
+    assert lib.qsa_sparse_attn_prefill_impl(ctypes.byref(c), None, None, None, 8, None, None, None, 0, 0, 16, 2,
+                                            0.0, None, None, 1, None) == 0

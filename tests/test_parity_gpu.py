@@ -280,10 +280,12 @@ def test_chunked_prefill_rows_at_offset():
     assert st["exact"] >= 0.98 * (hi - lo)
 
 
-def test_batched_prefill_sequences_at_different_offsets():
+@pytest.mark.parametrize("impl", ["auto", "tcgen05"])
+def test_batched_prefill_sequences_at_different_offsets(impl):
     """Three sequences in one call, each a 500-row chunk at its own position
     (0, 1100, 2100) against its own prefix: every (sequence, row) is checked
-    against the oracle run on that sequence alone."""
+    against the oracle run on that sequence alone, through each attention
+    kernel."""
     spec = PrefillSpec("b3", n=2600, k_tokens=512, seed=51, batch=3)
     wl = make_prefill(spec, DEV)
     cfg = cfg_for(spec)
@@ -300,7 +302,7 @@ def test_batched_prefill_sequences_at_different_offsets():
     qsa.qsa_index_topk(cfg, q_idx, kbar, q_pos, nb, idx, cnt, ws)
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=DEV)
-    qsa.qsa_sparse_attn_prefill(cfg, q, wl["k"], wl["v"], q_pos, idx, cnt, out, lse)
+    qsa.qsa_sparse_attn_prefill(cfg, q, wl["k"], wl["v"], q_pos, idx, cnt, out, lse, impl=impl)
     torch.cuda.synchronize()
     assert qsa.qsa_read_device_error() == 0
     rows = [0, 1, 250, 498, 499]
