@@ -371,34 +371,49 @@ topk_select_cluster_kernel(const float* __restrict__ S, int64_t s_stride, const 
       if (u[j] != 0xffffffffu) atomicAdd(&sm.base.hist[u[j] >> 20], 1);
   }
   cluster.sync();
-  // Merged histogram: this thread's 4 bins summed over the cluster.
-  const int base_bin = (kSelThreads - 1 - threadIdx.x) * kSelBinsPerThread;
-  int loc[kSelBinsPerThread] = {0, 0, 0, 0};
-  for (int q = 0; q < kSelCluster; ++q) {
-    const int* h = cluster.map_shared_rank(sm.base.hist, q);
+  // The first CTA merges the histograms (this thread's bins summed over the
+  // cluster), finds the boundary bin and hands it to the other CTAs; they wait
+  // at the cluster barrier instead of all reading each other's histograms.
+  if (rank == 0) {
+    const int base_bin = (kSelThreads - 1 - threadIdx.x) * kSelBinsPerThread;
+    int loc[kSelBinsPerThread];
 #pragma unroll
-    for (int j = 0; j < kSelBinsPerThread; ++j) loc[j] += h[base_bin + kSelBinsPerThread - 1 - j];
-  }
-  int sum = 0;
+    for (int j = 0; j < kSelBinsPerThread; ++j) loc[j] = 0;
 #pragma unroll
-  for (int j = 0; j < kSelBinsPerThread; ++j) sum += loc[j];
-  const int above0 = block_exclusive_scan(sum, sm.base.warp_sums, &sm.base.total);
-  if (above0 < k_b && above0 + sum >= k_b) {
-    int above = above0;
+    for (int q = 0; q < kSelCluster; ++q) {
+      const int* h = cluster.map_shared_rank(sm.base.hist, q);
 #pragma unroll
-    for (int j = 0; j < kSelBinsPerThread; ++j) {
-      if (above + loc[j] >= k_b) {
-        const int bin = base_bin + kSelBinsPerThread - 1 - j;
-        sm.base.lo = (uint32_t)bin << 20;
-        sm.base.hi = ((uint32_t)bin << 20) | 0xfffffu;
-        sm.base.need = k_b - above;
-        sm.base.done = above + loc[j];  // entries at or above the bin, whole row
-        break;
+      for (int j = 0; j < kSelBinsPerThread; ++j) loc[j] += h[base_bin + kSelBinsPerThread - 1 - j];
+    }
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < kSelBinsPerThread; ++j) sum += loc[j];
+    const int above0 = block_exclusive_scan(sum, sm.base.warp_sums, &sm.base.total);
+    if (above0 < k_b && above0 + sum >= k_b) {
+      int above = above0;
+#pragma unroll
+      for (int j = 0; j < kSelBinsPerThread; ++j) {
+        if (above + loc[j] >= k_b) {
+          const int bin = base_bin + kSelBinsPerThread - 1 - j;
+          sm.base.lo = (uint32_t)bin << 20;
+          sm.base.hi = ((uint32_t)bin << 20) | 0xfffffu;
+          sm.base.need = k_b - above;
+          sm.base.done = above + loc[j];  // entries at or above the bin, whole row
+          break;
+        }
+        above += loc[j];
       }
-      above += loc[j];
+    }
+    __syncthreads();
+    if (threadIdx.x > 0 && threadIdx.x < kSelCluster) {  // thread q writes CTA q's copy
+      SelectSmem* dst = cluster.map_shared_rank(&sm.base, (int)threadIdx.x);
+      dst->lo = sm.base.lo;
+      dst->hi = sm.base.hi;
+      dst->need = sm.base.need;
+      dst->done = sm.base.done;
     }
   }
-  cluster.sync();  // every CTA has read the others' histograms
+  cluster.sync();  // the boundary is in every CTA's shared memory; the histograms are no longer read
   const uint32_t lo = sm.base.lo, hi = sm.base.hi;
   const int need = sm.base.need;
   const int ncand = sm.base.done;
