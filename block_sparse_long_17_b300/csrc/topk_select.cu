@@ -471,13 +471,16 @@ topk_select_cluster_kernel(const float* __restrict__ S, int64_t s_stride, const 
   if (threadIdx.x == 0) count[row] = k_b;
 }
 
-// Clusters of 4 CTAs per row.  (Clusters of 8 were slower at 16 rows of
-// 262144 scores: the cluster barriers and the first CTA's refinement, not the
-// passes over the row, set the time.)
+// Clusters of 4 CTAs per row, or of 8 when fewer than 64 rows share the GPU
+// (a multi-token decode step of a few long sequences).
 cudaError_t launch_topk_select_cluster(const float* S, int64_t s_stride, const int64_t* q_pos, int64_t n_q,
                                        int64_t row_lo, int64_t n_rows, int r, int k_b, int64_t c_cap,
                                        int32_t* idx, int32_t* count, cudaStream_t st) {
   if (n_rows <= 0) return cudaSuccess;
+  if (n_rows < 64)
+    return count_launch(launch_dependent(topk_select_cluster_kernel<8>, dim3((unsigned)(n_rows * 8)),
+                                         dim3(kSelThreads), 0, st, S, s_stride, q_pos, n_q, row_lo, r, k_b, c_cap,
+                                         idx, count));
   return count_launch(launch_dependent(topk_select_cluster_kernel<4>, dim3((unsigned)(n_rows * 4)),
                                        dim3(kSelThreads), 0, st, S, s_stride, q_pos, n_q, row_lo, r, k_b, c_cap, idx,
                                        count));
