@@ -724,14 +724,41 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev, chunk: int = 16384) -> dict:
+def e2e_chunk_bounds(n: int, wave: int, r: int) -> list:
+    """Row bounds of the end-to-end prefill's chunks.  `wave`: rows of one wave of
+    the indexer (qsa_index_rows_per_wave).  Chunks of 1K, 2K and 4K rows and one
+    wave first (each chunk's copy-in fits inside the compute of the chunk before
+    it, so little of the host-to-device copy is exposed), then chunks of two
+    waves (whole waves for the indexer), then one wave and a quarter wave (the
+    copy-out after the last kernel stays short).  Any leftover rows form one
+    chunk after the first four.  Bounds are multiples of r except n."""
+    q = lambda x: max(r, x // r * r)
+    head = [q(x) for x in (1024, 2048, 4096, wave)]
+    tail = [q(wave), q(wave // 4)]
+    mid = q(2 * wave)
+    if sum(head) + sum(tail) >= n:  # short sequences: chunks of one wave
+        return list(range(0, n, q(wave))) + [n]
+    b = [0]
+    for x in head:
+        b.append(b[-1] + x)
+    k = (n - b[-1] - sum(tail)) // mid
+    rem = n - b[-1] - sum(tail) - k * mid
+    if rem > 0:
+        b.append(b[-1] + rem)
+    b += [b[-1] + mid * (j + 1) for j in range(k)]
+    for x in tail:
+        b.append(b[-1] + x)
+    return b
+
+
+def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev) -> dict:
     """The same step through the binding with host buffers: H2D of the step's
     inputs from pinned memory and D2H of its outputs, all inside the timed
-    region.  The prefill runs as chunked prefill (the pages' mode, 16K-row
-    chunks): one stream copies chunk i in, one computes it (compress its
-    blocks, select and attend its rows against the prefix), one copies its
-    output back, so that the copies of one chunk overlap the kernels of another.
-    The decode step follows on the compute stream."""
+    region.  The prefill runs as chunked prefill (the pages' mode) over the
+    chunks of e2e_chunk_bounds: one stream copies chunk i in, one computes it
+    (compress its blocks, select and attend its rows against the prefix), one
+    copies its output back, so that the copies of one chunk overlap the kernels
+    of another.  The decode step follows on the compute stream."""
     import torch
     host_in = {k: wl[k].cpu().pin_memory() for k in ("q_idx", "k_idx", "q", "k", "v")}
     dev_in = {k: torch.empty_like(wl[k]) for k in host_in}
@@ -743,14 +770,11 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev, chu
     h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + dq_h.numel() * 2 + dqi_h.numel() * 2
     d2h = out_h.numel() * 2 + dout_h.numel() * 2
     n, r, hkv = wl["q"].shape[1], cfg.r, wl["k"].shape[1]
-    # Chunk boundaries offset by half a chunk: the first chunk (whose copy-in
-    # the kernels wait for) is half-size, and so is the last one (whose
-    # copy-out follows them) when n is a multiple of the chunk.
-    bounds = [0] + list(range(min(n, chunk // 2), n, chunk)) + [n]
+    bounds = e2e_chunk_bounds(n, qsa.qsa_index_rows_per_wave(cfg), r)
     chunks = [(a, b) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
     qpos = [torch.full((1,), lo, dtype=torch.int64, device=dev) for lo, _ in chunks]
-    ws_c = torch.empty((qsa.qsa_index_topk_workspace(cfg, 1, min(chunk, n), pre.n_blocks),), dtype=torch.uint8,
-                       device=dev)
+    ws_c = torch.empty((qsa.qsa_index_topk_workspace(cfg, 1, max(b - a for a, b in chunks), pre.n_blocks),),
+                       dtype=torch.uint8, device=dev)
     s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     main = torch.cuda.current_stream(dev)
     torch.cuda.synchronize()
@@ -816,7 +840,7 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev, chu
     same = bool(torch.equal(out_h.to(dev), ref))
     return {"value": n / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "chunk_tokens": chunk, "output_matches_device_step": same,
+            "chunk_rows": [b - a for a, b in chunks], "output_matches_device_step": same,
             "steps": k,
             "note": "tokens/s of the prefill sequence over the whole step incl. copies and decode; chunked "
                     "prefill with copies on their own streams; the decode step's state (16 GiB K/V cache and "

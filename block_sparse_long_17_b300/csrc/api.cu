@@ -138,6 +138,19 @@ size_t qsa_index_topk_workspace(const qsa_config* cfg, int64_t B, int64_t n_q, i
   return index_layout(B, n_q, n_blocks_max, k_blocks(cfg), cfg->n_idx_heads).total;
 }
 
+qsa_status qsa_index_rows_per_wave(const qsa_config* cfg, int64_t* rows) {
+  qsa_status s = check_config(cfg);
+  if (s != QSA_OK) return s;
+  if (rows == nullptr) return QSA_ERR_INVALID_ARG;
+  int sms = 0;
+  if (current_sm_count(&sms) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();  // a failed query leaves no sticky error behind
+    return QSA_ERR_CUDA;
+  }
+  *rows = (int64_t)fused_tile_tokens(cfg->n_idx_heads) * sms;
+  return QSA_OK;
+}
+
 qsa_status qsa_index_topk(const qsa_config* cfg, const void* q_idx, const void* kbar,
                           int64_t kbar_stride_b, const int64_t* q_pos, int64_t B, int64_t n_q,
                           int64_t n_blocks_max, int32_t* idx, int32_t* count, void* ws,

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED",
 
 EXPORTED = [
     "qsa_default_config", "qsa_num_selected_blocks", "qsa_compress_keys",
-    "qsa_index_topk_workspace", "qsa_index_topk", "qsa_index_topk_fallback_rows", "qsa_sparse_attn_prefill",
+    "qsa_index_topk_workspace", "qsa_index_rows_per_wave", "qsa_index_topk", "qsa_index_topk_fallback_rows",
+    "qsa_sparse_attn_prefill",
     "qsa_sparse_attn_prefill_impl",
     "qsa_sparse_attn_decode_workspace", "qsa_sparse_attn_decode", "qsa_sparse_attn_decode_noalloc",
     "qsa_sparse_attn_decode_multi_workspace", "qsa_sparse_attn_decode_multi",
@@ -89,6 +90,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qsa_num_selected_blocks": (I32, [C]),
         "qsa_compress_keys": (ctypes.c_int, [C, P, I64, I64, I64, I64, P, I64, P]),
         "qsa_index_topk_workspace": (SZ, [C, I64, I64, I64]),
+        "qsa_index_rows_per_wave": (ctypes.c_int, [C, ctypes.POINTER(I64)]),
         "qsa_index_topk": (ctypes.c_int, [C, P, P, I64, P, I64, I64, I64, P, P, P, SZ, P]),
         "qsa_index_topk_fallback_rows": (ctypes.c_int, [C, I64, I64, I64, P, SZ, ctypes.POINTER(I64), P]),
         "qsa_sparse_attn_prefill": (ctypes.c_int, [C, P, P, P, I64, P, P, P, I64, I64, I32, I32, F, P, P, P]),
@@ -172,6 +174,15 @@ def qsa_index_topk(cfg: Config, q_idx: torch.Tensor, kbar: torch.Tensor, q_pos: 
     _check("qsa_index_topk", load_library().qsa_index_topk(
         ctypes.byref(c), _ptr(q_idx), _ptr(kbar), kbar.stride(0), _ptr(q_pos), B, n_q, n_blocks_max,
         _ptr(idx), _ptr(count), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def qsa_index_rows_per_wave(cfg: Config) -> int:
+    """Query rows one wave of the prefill indexer covers on the current device
+    (a chunk-size hint for chunked prefill)."""
+    c = cfg.c_struct()
+    rows = ctypes.c_int64(0)
+    _check("qsa_index_rows_per_wave", load_library().qsa_index_rows_per_wave(ctypes.byref(c), ctypes.byref(rows)))
+    return int(rows.value)
 
 
 def qsa_index_topk_fallback_rows(cfg: Config, B: int, n_q: int, n_blocks_max: int, ws: torch.Tensor,

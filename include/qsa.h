@@ -118,6 +118,20 @@ size_t qsa_index_topk_workspace(const qsa_config* cfg, int64_t B, int64_t n_q,
                                 int64_t n_blocks_max);
 
 /*
+ * Query rows that one wave of the prefill indexer covers on the current device:
+ * its tile rows (48; 24 with 8 indexer heads) times the device's SM count.  A
+ * qsa_index_topk call over n_q rows of one sequence runs ceil(n_q / tile rows)
+ * tiles, at most one per SM at a time, so chunked prefill [QSA] ("chunked
+ * prefill" of the decode/prefill panels) with chunk sizes that are multiples of
+ * this number keeps every SM busy to the end of each indexer launch.  A
+ * sizing hint only: every chunk size gives the same result.
+ *   rows  host int64 out.
+ * Returns QSA_ERR_INVALID_ARG for a null cfg or rows, QSA_ERR_UNSUPPORTED for
+ * an unsupported cfg, QSA_ERR_CUDA when the device cannot be queried (no GPU).
+ */
+qsa_status qsa_index_rows_per_wave(const qsa_config* cfg, int64_t* rows);
+
+/*
  * Indexer scoring and top-k_B block selection [KI], [QSA] steps 3-4:
  *   I_ib = sum_{h < H} ReLU(<qt_i^h, kbar_b>)   for b < c_i,  H = n_idx_heads,
  * where qt_i^h = bf16(RoPE_{floor(i/r)}(q_idx[i, h])).  For each row, if

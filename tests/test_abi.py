@@ -162,3 +162,21 @@ def test_attention_kernel_choice_checked_on_the_host(lib):
     # empty work succeeds without a launch
     assert lib.qsa_sparse_attn_prefill_impl(ctypes.byref(c), None, None, None, 8, None, None, None, 0, 0, 16, 2,
                                             0.0, None, None, 1, None) == 0
+
+
+def test_rows_per_wave_checks_arguments(lib):
+    """qsa_index_rows_per_wave: bad arguments are refused before the device is
+    queried; without a GPU the query itself reports QSA_ERR_CUDA and leaves the
+    output untouched."""
+    import torch
+    c = _cfg()
+    rows = ctypes.c_int64(-7)
+    assert lib.qsa_index_rows_per_wave(None, ctypes.byref(rows)) == 1
+    assert lib.qsa_index_rows_per_wave(ctypes.byref(c), None) == 1
+    bad = _cfg()
+    bad.n_idx_heads = 3
+    assert lib.qsa_index_rows_per_wave(ctypes.byref(bad), ctypes.byref(rows)) == 2
+    assert rows.value == -7
+    if not torch.cuda.is_available():
+        assert lib.qsa_index_rows_per_wave(ctypes.byref(c), ctypes.byref(rows)) == 4
+        assert rows.value == -7

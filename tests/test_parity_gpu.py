@@ -280,6 +280,51 @@ def test_chunked_prefill_rows_at_offset():
     assert st["exact"] >= 0.98 * (hi - lo)
 
 
+def test_rows_per_wave_and_chunks_of_it_match_the_one_call_prefill():
+    """qsa_index_rows_per_wave is the indexer's tile rows times the SM count.  A
+    prefill run as chunks shaped like the end-to-end pipeline's (small chunks
+    first, then one wave's rows, then the rest) selects the same blocks and
+    writes the same output, bit for bit, as the one-call prefill: every chunk
+    of at least 64 rows takes the fused indexer, whose selection is exact
+    whatever tiles the chunk makes, and each row's attention depends on that
+    row alone."""
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    wave = qsa.qsa_index_rows_per_wave(qsa.Config())
+    assert wave == 48 * sms
+    assert qsa.qsa_index_rows_per_wave(qsa.Config(n_idx_heads=8)) == 24 * sms
+    n = 7168 + wave + 3000
+    spec = PrefillSpec("w", n=n, k_tokens=2048, seed=14, drift=True)
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    one = run_prefill(cfg, wl)
+    bounds = [0, 1024, 3072, 7168, 7168 + wave, n]
+    nb = n // cfg.r
+    kbar = torch.empty((1, nb, 128), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty((1, n, cfg.k_b), dtype=torch.int32, device=DEV)
+    cnt = torch.empty((1, n), dtype=torch.int32, device=DEV)
+    out = torch.empty_like(wl["q"])
+    lse = torch.empty(wl["q"].shape[:3], dtype=torch.float32, device=DEV)
+    ws = torch.empty((qsa.qsa_index_topk_workspace(cfg, 1, max(b - a for a, b in zip(bounds, bounds[1:])), nb),),
+                     dtype=torch.uint8, device=DEV)
+    fallback = 0
+    for lo, hi in zip(bounds, bounds[1:]):
+        q_pos = torch.full((1,), lo, dtype=torch.int64, device=DEV)
+        qsa.qsa_compress_keys(cfg, wl["k_idx"], lo // cfg.r, hi // cfg.r - lo // cfg.r, kbar)
+        qsa.qsa_index_topk(cfg, wl["q_idx"][:, lo:hi], kbar, q_pos, hi // cfg.r, idx[:, lo:hi], cnt[:, lo:hi], ws)
+        fallback += qsa.qsa_index_topk_fallback_rows(cfg, 1, hi - lo, hi // cfg.r, ws)
+        qsa.qsa_sparse_attn_prefill(cfg, wl["q"][:, lo:hi], wl["k"], wl["v"], q_pos, idx[:, lo:hi],
+                                    cnt[:, lo:hi], out[:, lo:hi], lse[:, lo:hi])
+    torch.cuda.synchronize()
+    assert qsa.qsa_read_device_error() == 0
+    # A row of the exact fallback is scored by another MMA instruction, whose fp32
+    # sums may round differently; this workload sends no row there.
+    assert one["fallback_rows"] == 0 and fallback == 0
+    assert np.array_equal(cnt.cpu().numpy(), one["count"])
+    assert np.array_equal(idx.cpu().numpy(), one["idx"])
+    assert np.array_equal(out.float().cpu().numpy(), one["out"])
+    assert np.array_equal(lse.cpu().numpy(), one["lse"])
+
+
 @pytest.mark.parametrize("impl", ["auto", "tcgen05"])
 def test_batched_prefill_sequences_at_different_offsets(impl):
     """Three sequences in one call, each a 500-row chunk at its own position
