@@ -6,7 +6,7 @@
 #include <stdint.h>
 
 #include <mutex>
-#include <set>
+#include <map>
 #include <utility>
 
 #include "../../include/qsa.h"
@@ -46,23 +46,26 @@ inline cudaError_t count_launch(cudaError_t e) {
   return e;
 }
 
-// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
-// device, once per (kernel, device): the attribute belongs to each device's
-// copy of the kernel, so a process that drives several GPUs sets it on each.
+// Raises `kernel`'s dynamic shared-memory limit to at least `bytes` on the
+// current device.  The limit set is remembered per (kernel, device), and a
+// call that needs more raises it again (a kernel whose shared memory depends
+// on its arguments); the attribute belongs to each device's copy of the
+// kernel, so a process that drives several GPUs sets it on each.
 inline cudaError_t ensure_dyn_smem(const void* kernel, int bytes) {
   static std::mutex mu;
-  static std::set<std::pair<const void*, int>> done;
+  static std::map<std::pair<const void*, int>, int> set_to;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (done.count({kernel, dev})) return cudaSuccess;
+  const auto it = set_to.find({kernel, dev});
+  if (it != set_to.end() && it->second >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   // All of the unified L1/shared storage as shared memory, so that the
   // occupancy the kernel was sized for (for some kernels two CTAs per SM) is
   // available.
   if (e == cudaSuccess) e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-  if (e == cudaSuccess) done.insert({kernel, dev});
+  if (e == cudaSuccess) set_to[{kernel, dev}] = bytes;
   return e;
 }
 
