@@ -15,7 +15,11 @@
 // 3-stage cp.async ring in shared memory (16 tokens = 8 KB of K and V per
 // stage, 16-byte chunks XOR-swizzled by row so that ldmatrix reads are free of
 // bank conflicts), so two stages of loads are always in flight while the third
-// is consumed.  Per stage the warp computes S^T = K Q^T with m16n8k16 MMAs
+// is consumed.  The item's selected block ids are copied once into a
+// 512-entry window in the warp's shared memory (one coalesced load, repeated
+// only past 512 blocks), so a stage's copies are issued after a shared-memory
+// read rather than after an L2 round trip; block and slot arithmetic uses
+// shifts (r is a power of two).  Per stage the warp computes S^T = K Q^T with m16n8k16 MMAs
 // (16 tokens x 8 heads; K fragments by ldmatrix), an fp32 online softmax per
 // head, and O^T += V^T P^T (V fragments by ldmatrix.trans, P transposed by
 // movmatrix).
@@ -27,8 +31,10 @@ constexpr int kAWarps = 8;                                   // warps per CTA
 constexpr int kARing = 3;                                    // cp.async stages per warp
 constexpr int kAGroup = 16;                                  // gathered tokens per stage
 constexpr int kAStageBytes = kAGroup * 2 * kHeadDim * 2;     // K and V rows: 8 KB
-constexpr int kAWarpBytes = kARing * kAStageBytes;           // 24 KB
-constexpr int kASmemBytes = kAWarps * kAWarpBytes;           // 192 KB
+constexpr int kAIds = 512;                                   // block ids per window
+constexpr int kARingBytes = kARing * kAStageBytes;           // 24 KB
+constexpr int kAWarpBytes = kARingBytes + kAIds * 4;         // 26 KB: ring, then the id window
+constexpr int kASmemBytes = kAWarps * kAWarpBytes;           // 208 KB
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnRow {
@@ -36,26 +42,47 @@ struct AttnRow {
   int64_t c;       // completed blocks visible
   int cnt;         // selected blocks
   int n_tok;       // |T_i| = cnt * r + tail
+  int rs;          // log2 r (r is a power of two): slot / r and slot % r by shift and mask
   const int32_t* sel;
 };
 
-__device__ __forceinline__ int64_t slot_token(const AttnRow& a, int r, int slot) {
-  const int sel_tok = a.cnt * r;
+// Block ids [w0, w0 + kAIds) of the row's selection into the warp's window
+// `ids` (shared memory); entries past cnt are 0.
+__device__ __forceinline__ void load_id_window(int32_t* ids, const AttnRow& a, int w0) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();  // every lane is done with the previous window
+  int32_t v[kAIds / 32];
+#pragma unroll
+  for (int j = 0; j < kAIds / 32; ++j) {
+    const int b = w0 + lane + 32 * j;
+    v[j] = b < a.cnt ? __ldg(a.sel + b) : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < kAIds / 32; ++j) ids[lane + 32 * j] = v[j];
+  __syncwarp();
+}
+
+// slot_token with the selected block ids read from the window that starts at
+// block w0 (every selected slot asked for has slot / r - w0 in [0, kAIds)).
+__device__ __forceinline__ int64_t slot_token_window(const AttnRow& a, int r, int slot, const int32_t* ids,
+                                                     int w0) {
+  const int sel_tok = a.cnt << a.rs;
   if (slot < sel_tok) {
-    int64_t b = __ldg(a.sel + slot / r);
+    int64_t b = ids[(slot >> a.rs) - w0];
     if ((uint64_t)b >= (uint64_t)a.c) {  // malformed selection: read block 0, report
       flag_device_error(kDevErrBlockId);
       b = 0;
     }
-    return b * r + (slot % r);
+    return (b << a.rs) + (slot & (r - 1));
   }
-  return a.c * r + (slot - sel_tok);
+  return (a.c << a.rs) + (slot - sel_tok);
 }
 
 __device__ __forceinline__ AttnRow make_row(int64_t i, int r, const int32_t* sel, int cnt, int k_b) {
   AttnRow a;
   a.i = i;
-  a.c = (i + 1) / r;
+  a.rs = __ffs(r) - 1;
+  a.c = (i + 1) >> a.rs;
   const int64_t cmax = a.c < k_b ? a.c : k_b;
   if (cnt < 0 || cnt > cmax) {  // count inconsistent with the position: clamp, report
     flag_device_error(kDevErrBlockId);
@@ -63,7 +90,7 @@ __device__ __forceinline__ AttnRow make_row(int64_t i, int r, const int32_t* sel
   }
   a.cnt = cnt;
   a.sel = sel;
-  a.n_tok = cnt * r + (int)(i + 1 - a.c * r);
+  a.n_tok = (cnt << a.rs) + (int)(i + 1 - (a.c << a.rs));
   return a;
 }
 
@@ -98,11 +125,11 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // 16 bytes per lane), so every request is a full, contiguous 256-byte row.
 __device__ __forceinline__ void issue_stage(uint32_t kst, const AttnRow& a, int r, int s0, int slot_end,
                                             const __nv_bfloat16* __restrict__ kh,
-                                            const __nv_bfloat16* __restrict__ vh) {
+                                            const __nv_bfloat16* __restrict__ vh, const int32_t* ids, int w0) {
   const int lane = threadIdx.x & 31;
   int slot = s0 + (lane & 15);
   if (slot >= slot_end) slot = slot_end - 1;
-  const int64_t my_tok = slot_token(a, r, slot);  // token of row lane % 16
+  const int64_t my_tok = slot_token_window(a, r, slot, ids, w0);  // token of row lane % 16
   const int chunk = lane & 15, sub = lane >> 4;
   const uint32_t vst = kst + kAGroup * 256;
 #pragma unroll
@@ -116,7 +143,8 @@ __device__ __forceinline__ void issue_stage(uint32_t kst, const AttnRow& a, int 
 
 // Attention of one token (row `a`) for 8 query heads (qh0 .. qh0+7, only the
 // first n_heads valid) over gathered slots [slot_beg, slot_end), slot_beg <
-// slot_end.  `ring` is the warp's kARing-stage buffer (shared-window address).
+// slot_end.  `ring` is the warp's kARing-stage buffer (shared-window address),
+// `ids` its block-id window.
 // Results per lane: o[mt][e] = unnormalised O^T (dims 16 mt + gid (+8), heads
 // 2t, 2t+1), running max m2[2] (log2 units, scale folded in) and sum l[2] of
 // the lane's heads 2t, 2t+1 (reduced across the warp).
@@ -124,12 +152,27 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
                                              const __nv_bfloat16* __restrict__ kh,
                                              const __nv_bfloat16* __restrict__ vh, const AttnRow& a,
                                              int r, int slot_beg, int slot_end, float scale_log2,
-                                             uint32_t ring, float o[8][4], float m2[2], float l[2]) {
+                                             uint32_t ring, int32_t* ids, float o[8][4], float m2[2], float l[2]) {
   const int lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
   const int ngroups = (slot_end - slot_beg + kAGroup - 1) / kAGroup;
+  // The window holds blocks [w0, w0 + kAIds); a stage whose selected slots
+  // reach past it moves it to the stage's first block (stages only advance,
+  // so no later stage asks for a block below w0).
+  const int sel_tok = a.cnt << a.rs;
+  int w0 = slot_beg >> a.rs;
+  load_id_window(ids, a, w0);
+  auto issue = [&](int gi) {
+    const int s0 = slot_beg + gi * kAGroup;
+    const int last = min(s0 + kAGroup, min(slot_end, sel_tok)) - 1;
+    if (last >= s0 && (last >> a.rs) >= w0 + kAIds) {
+      w0 = s0 >> a.rs;
+      load_id_window(ids, a, w0);
+    }
+    issue_stage(ring + (gi % kARing) * kAStageBytes, a, r, s0, slot_end, kh, vh, ids, w0);
+  };
 #pragma unroll
   for (int p = 0; p < kARing - 1; ++p) {
-    if (p < ngroups) issue_stage(ring + p * kAStageBytes, a, r, slot_beg + p * kAGroup, slot_end, kh, vh);
+    if (p < ngroups) issue(p);
     cp_async_commit();
   }
   // B fragments of Q^T: lane holds head gid, dims 16 ks + 2t (+1) and + 8.
@@ -152,7 +195,7 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
 
   for (int g = 0; g < ngroups; ++g) {
     const int gi = g + kARing - 1;
-    if (gi < ngroups) issue_stage(ring + (gi % kARing) * kAStageBytes, a, r, slot_beg + gi * kAGroup, slot_end, kh, vh);
+    if (gi < ngroups) issue(gi);
     cp_async_commit();
     cp_async_wait<kARing - 1>();
     __syncwarp();
@@ -241,6 +284,7 @@ sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
   uint8_t* const wbuf = attn_smem + warp * kAWarpBytes;
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(wbuf));
+  int32_t* const ids = reinterpret_cast<int32_t*>(wbuf + kARingBytes);
   const int group = Hq / Hkv;
   const int n_hc = (group + 7) / 8;
   const int64_t per_head = B * n_q * n_hc;
@@ -263,7 +307,7 @@ sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
     const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
     const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
     float o[8][4], m2[2], l[2];
-    attend_slots(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, 0, a.n_tok, scale * kLog2e, ring, o,
+    attend_slots(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, 0, a.n_tok, scale * kLog2e, ring, ids, o,
                  m2, l);
     float* st = reinterpret_cast<float*>(wbuf);
     stage_o(st, o, 1.f / l[0], 1.f / l[1]);
@@ -361,6 +405,7 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
   uint8_t* const wbuf = attn_smem + warp * kAWarpBytes;
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(wbuf));
+  int32_t* const ids = reinterpret_cast<int32_t*>(wbuf + kARingBytes);
   const int group = Hq / Hkv;
   const int n_hc = (group + 7) / 8;
   const int64_t items = B * n_q * Hkv * n_hc * n_split;
@@ -395,7 +440,7 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
       const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
       const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
       float o[8][4], m2[2], l[2];
-      attend_slots(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end, scale * kLog2e, ring, o,
+      attend_slots(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end, scale * kLog2e, ring, ids, o,
                    m2, l);
       float* st = reinterpret_cast<float*>(wbuf);
       stage_o(st, o, 1.f, 1.f);
