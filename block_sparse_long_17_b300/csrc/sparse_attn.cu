@@ -10,19 +10,22 @@
 // Work item = (query token, kv head, chunk of 8 query heads of that group), one
 // warp each; warps are persistent and take items in an order that keeps one kv
 // head's K/V hot in L2.  The per-token selection gives no reuse across tokens,
-// so the kernel is bound by gathering 512 B of K and V per selected token and
-// kv head from L2/HBM.  Each warp streams its gathered rows through its own
-// 3-stage cp.async ring in shared memory (16 tokens = 8 KB of K and V per
-// stage, 16-byte chunks XOR-swizzled by row so that ldmatrix reads are free of
-// bank conflicts), so two stages of loads are always in flight while the third
-// is consumed.  The item's selected block ids are copied once into a
-// 512-entry window in the warp's shared memory (one coalesced load, repeated
-// only past 512 blocks), so a stage's copies are issued after a shared-memory
-// read rather than after an L2 round trip; block and slot arithmetic uses
-// shifts (r is a power of two).  Per stage the warp computes S^T = K Q^T with m16n8k16 MMAs
-// (16 tokens x 8 heads; K fragments by ldmatrix), an fp32 online softmax per
-// head, and O^T += V^T P^T (V fragments by ldmatrix.trans, P transposed by
-// movmatrix).
+// so the kernel moves 512 B of K and V per selected token and kv head from
+// L2/HBM.  Each warp streams its gathered rows through its own 3-stage cp.async
+// ring in shared memory (16 tokens = 8 KB of K and V per stage, 16-byte chunks
+// XOR-swizzled by row so that ldmatrix reads are free of bank conflicts), so
+// two stages of loads are always in flight while the third is consumed.  With
+// eight such warps per SM the kernel is bound by each warp's instructions and
+// dependent latencies per stage, so the stage is kept lean:
+//   * the item's selected block ids are copied once into a 512-entry window in
+//     the warp's shared memory (one coalesced load, repeated only past 512
+//     blocks, ids checked there), so a stage's copies are issued after a
+//     shared-memory read rather than after an L2 round trip;
+//   * block and slot arithmetic uses shifts (r is a power of two);
+//   * S^T = K Q^T (m16n8k16 MMAs, 16 tokens x 8 heads, K fragments by
+//     ldmatrix) runs its 8 k-steps as two accumulator chains of 4, summed.
+// Then an fp32 online softmax per head, and O^T += V^T P^T (V fragments by
+// ldmatrix.trans, P transposed by movmatrix).
 #include "common.cuh"
 
 namespace qsa {
@@ -47,7 +50,8 @@ struct AttnRow {
 };
 
 // Block ids [w0, w0 + kAIds) of the row's selection into the warp's window
-// `ids` (shared memory); entries past cnt are 0.
+// `ids` (shared memory); entries past cnt are 0.  An id outside [0, c) is
+// reported and replaced by block 0 here, once per item, not per stage.
 __device__ __forceinline__ void load_id_window(int32_t* ids, const AttnRow& a, int w0) {
   const int lane = threadIdx.x & 31;
   __syncwarp();  // every lane is done with the previous window
@@ -56,6 +60,13 @@ __device__ __forceinline__ void load_id_window(int32_t* ids, const AttnRow& a, i
   for (int j = 0; j < kAIds / 32; ++j) {
     const int b = w0 + lane + 32 * j;
     v[j] = b < a.cnt ? __ldg(a.sel + b) : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < kAIds / 32; ++j) {
+    if (w0 + lane + 32 * j < a.cnt && (uint32_t)v[j] >= (uint64_t)a.c) {  // malformed: read block 0, report
+      flag_device_error(kDevErrBlockId);
+      v[j] = 0;
+    }
   }
 #pragma unroll
   for (int j = 0; j < kAIds / 32; ++j) ids[lane + 32 * j] = v[j];
@@ -68,11 +79,7 @@ __device__ __forceinline__ int64_t slot_token_window(const AttnRow& a, int r, in
                                                      int w0) {
   const int sel_tok = a.cnt << a.rs;
   if (slot < sel_tok) {
-    int64_t b = ids[(slot >> a.rs) - w0];
-    if ((uint64_t)b >= (uint64_t)a.c) {  // malformed selection: read block 0, report
-      flag_device_error(kDevErrBlockId);
-      b = 0;
-    }
+    const int64_t b = ids[(slot >> a.rs) - w0];  // checked against c when loaded
     return (b << a.rs) + (slot & (r - 1));
   }
   return (a.c << a.rs) + (slot - sel_tok);
@@ -204,13 +211,17 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
     const int s0 = slot_beg + g * kAGroup;
     const bool va_ok = s0 + gid < slot_end, vb_ok = s0 + gid + 8 < slot_end;
 
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};  // k-steps 0, 2, 4, 6 | 1, 3, 5, 7
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t af[4];
+    for (int ks = 0; ks < 8; ks += 2) {
+      uint32_t af[4], ag[4];
       ldsm_x4(kst + swz(krow, 2 * ks + kchk), af);
+      ldsm_x4(kst + swz(krow, 2 * ks + 2 + kchk), ag);
       mma_bf16_16816(sc, af, qf[ks]);
+      mma_bf16_16816(sd, ag, qf[ks + 1]);
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[e] += sd[e];
     // sc: (slot s0+gid, head 2t), (s0+gid, 2t+1), (s0+gid+8, 2t), (s0+gid+8, 2t+1)
     const float x0 = va_ok ? sc[0] * scale_log2 : -INFINITY;
     const float x1 = va_ok ? sc[1] * scale_log2 : -INFINITY;
