@@ -11,12 +11,13 @@
 // warp each; warps are persistent and take items in an order that keeps one kv
 // head's K/V hot in L2.  The per-token selection gives no reuse across tokens,
 // so the kernel moves 512 B of K and V per selected token and kv head from
-// L2/HBM.  Each warp streams its gathered rows through its own 3-stage cp.async
-// ring in shared memory (16 tokens = 8 KB of K and V per stage, 16-byte chunks
-// XOR-swizzled by row so that ldmatrix reads are free of bank conflicts), so
-// two stages of loads are always in flight while the third is consumed.  With
-// eight such warps per SM the kernel is bound by each warp's instructions and
-// dependent latencies per stage, so the stage is kept lean:
+// L2/HBM.  Each warp streams its gathered rows through its own cp.async ring in
+// shared memory (16 tokens = 8 KB of K and V per stage, 16-byte chunks
+// XOR-swizzled by row so that ldmatrix reads are free of bank conflicts): the
+// ring's other stages are in flight while one is consumed.  Prefill runs
+// twelve warps per SM with two stages each, decode eight with three (see
+// AttnShape).  The warps are bound by their instructions and dependent
+// latencies per stage, so the stage is kept lean:
 //   * the item's selected block ids are copied once into a 512-entry window in
 //     the warp's shared memory (one coalesced load, repeated only past 512
 //     blocks, ids checked there), so a stage's copies are issued after a
@@ -30,14 +31,26 @@
 
 namespace qsa {
 
-constexpr int kAWarps = 8;                                   // warps per CTA
-constexpr int kARing = 3;                                    // cp.async stages per warp
 constexpr int kAGroup = 16;                                  // gathered tokens per stage
 constexpr int kAStageBytes = kAGroup * 2 * kHeadDim * 2;     // K and V rows: 8 KB
 constexpr int kAIds = 512;                                   // block ids per window
-constexpr int kARingBytes = kARing * kAStageBytes;           // 24 KB
-constexpr int kAWarpBytes = kARingBytes + kAIds * 4;         // 26 KB: ring, then the id window
-constexpr int kASmemBytes = kAWarps * kAWarpBytes;           // 208 KB
+
+// Per-kernel shape: warps per CTA (one CTA per SM) and cp.async stages per
+// warp; each warp's shared memory is its ring, then its id window.  Prefill
+// gathers from L2 and is bound by each warp's per-stage dependencies, which
+// twelve warps of two stages hide better than eight of three (measured 15.5
+// against 18.9 ms at 128K); decode streams from HBM, where three stages per
+// warp keep more bytes in flight (the twelve-warp shape was 14% slower there).
+template <int kWarps_, int kRing_>
+struct AttnShape {
+  static constexpr int kWarps = kWarps_, kRing = kRing_;
+  static constexpr int kRingBytes = kRing * kAStageBytes;
+  static constexpr int kWarpBytes = kRingBytes + kAIds * 4;
+  static constexpr int kSmemBytes = kWarps * kWarpBytes;
+};
+using PrefillShape = AttnShape<12, 2>;  // 216 KB
+using DecodeShape = AttnShape<8, 3>;    // 208 KB
+static_assert(PrefillShape::kSmemBytes <= 227 * 1024 && DecodeShape::kSmemBytes <= 227 * 1024, "shared memory");
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnRow {
@@ -150,11 +163,12 @@ __device__ __forceinline__ void issue_stage(uint32_t kst, const AttnRow& a, int 
 
 // Attention of one token (row `a`) for 8 query heads (qh0 .. qh0+7, only the
 // first n_heads valid) over gathered slots [slot_beg, slot_end), slot_beg <
-// slot_end.  `ring` is the warp's kARing-stage buffer (shared-window address),
+// slot_end.  `ring` is the warp's kRing-stage buffer (shared-window address),
 // `ids` its block-id window.
 // Results per lane: o[mt][e] = unnormalised O^T (dims 16 mt + gid (+8), heads
 // 2t, 2t+1), running max m2[2] (log2 units, scale folded in) and sum l[2] of
 // the lane's heads 2t, 2t+1 (reduced across the warp).
+template <int kRing>
 __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q_heads, int n_heads,
                                              const __nv_bfloat16* __restrict__ kh,
                                              const __nv_bfloat16* __restrict__ vh, const AttnRow& a,
@@ -175,10 +189,10 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
       w0 = s0 >> a.rs;
       load_id_window(ids, a, w0);
     }
-    issue_stage(ring + (gi % kARing) * kAStageBytes, a, r, s0, slot_end, kh, vh, ids, w0);
+    issue_stage(ring + (gi % kRing) * kAStageBytes, a, r, s0, slot_end, kh, vh, ids, w0);
   };
 #pragma unroll
-  for (int p = 0; p < kARing - 1; ++p) {
+  for (int p = 0; p < kRing - 1; ++p) {
     if (p < ngroups) issue(p);
     cp_async_commit();
   }
@@ -201,12 +215,12 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
   const int vrow = ri + 8 * (mi >> 1), vchk = mi & 1;   // V: tokens 0-15, chunk 2 mt + vchk
 
   for (int g = 0; g < ngroups; ++g) {
-    const int gi = g + kARing - 1;
+    const int gi = g + kRing - 1;
     if (gi < ngroups) issue(gi);
     cp_async_commit();
-    cp_async_wait<kARing - 1>();
+    cp_async_wait<kRing - 1>();
     __syncwarp();
-    const uint32_t kst = ring + (g % kARing) * kAStageBytes;
+    const uint32_t kst = ring + (g % kRing) * kAStageBytes;
     const uint32_t vst = kst + kAGroup * 256;
     const int s0 = slot_beg + g * kAGroup;
     const bool va_ok = s0 + gid < slot_end, vb_ok = s0 + gid + 8 < slot_end;
@@ -284,7 +298,7 @@ __device__ __forceinline__ void stage_o(float* st, const float o[8][4], float s0
 
 // Prefill: persistent warps over (kv head, token, 8-head chunk) items, kv head
 // outermost so that concurrently running warps gather from one head's K/V.
-__global__ void __launch_bounds__(kAWarps * 32, 1)
+__global__ void __launch_bounds__(PrefillShape::kWarps * 32, 1)
 sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                            const __nv_bfloat16* __restrict__ v, int64_t L_cap,
                            const int64_t* __restrict__ q_pos, const int32_t* __restrict__ idx,
@@ -293,15 +307,15 @@ sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
                            float* __restrict__ lse) {
   extern __shared__ __align__(128) uint8_t attn_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
-  uint8_t* const wbuf = attn_smem + warp * kAWarpBytes;
+  uint8_t* const wbuf = attn_smem + warp * PrefillShape::kWarpBytes;
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(wbuf));
-  int32_t* const ids = reinterpret_cast<int32_t*>(wbuf + kARingBytes);
+  int32_t* const ids = reinterpret_cast<int32_t*>(wbuf + PrefillShape::kRingBytes);
   const int group = Hq / Hkv;
   const int n_hc = (group + 7) / 8;
   const int64_t per_head = B * n_q * n_hc;
   const int64_t items = per_head * Hkv;
-  const int64_t nwarps = (int64_t)gridDim.x * kAWarps;
-  for (int64_t item = (int64_t)blockIdx.x * kAWarps + warp; item < items; item += nwarps) {
+  const int64_t nwarps = (int64_t)gridDim.x * PrefillShape::kWarps;
+  for (int64_t item = (int64_t)blockIdx.x * PrefillShape::kWarps + warp; item < items; item += nwarps) {
     const int g = (int)(item / per_head);
     const int64_t rem = item % per_head;
     const int64_t row = rem / n_hc;
@@ -318,7 +332,7 @@ sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
     const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
     const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
     float o[8][4], m2[2], l[2];
-    attend_slots(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, 0, a.n_tok, scale * kLog2e, ring, ids, o,
+    attend_slots<PrefillShape::kRing>(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, 0, a.n_tok, scale * kLog2e, ring, ids, o,
                  m2, l);
     float* st = reinterpret_cast<float*>(wbuf);
     stage_o(st, o, 1.f / l[0], 1.f / l[1]);
@@ -403,7 +417,7 @@ __device__ void combine_unit(const float* __restrict__ po_unit, const float* __r
   }
 }
 
-__global__ void __launch_bounds__(kAWarps * 32, 1)
+__global__ void __launch_bounds__(DecodeShape::kWarps * 32, 1)
 sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                           const __nv_bfloat16* __restrict__ v, int64_t L_cap,
                           const int64_t* __restrict__ cache_len, const int32_t* __restrict__ idx,
@@ -414,14 +428,14 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
   extern __shared__ __align__(128) uint8_t attn_smem[];
   griddep_wait();  // the selection and the zeroed counters come from the previous kernels
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, t = lane & 3;
-  uint8_t* const wbuf = attn_smem + warp * kAWarpBytes;
+  uint8_t* const wbuf = attn_smem + warp * DecodeShape::kWarpBytes;
   const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(wbuf));
-  int32_t* const ids = reinterpret_cast<int32_t*>(wbuf + kARingBytes);
+  int32_t* const ids = reinterpret_cast<int32_t*>(wbuf + DecodeShape::kRingBytes);
   const int group = Hq / Hkv;
   const int n_hc = (group + 7) / 8;
   const int64_t items = B * n_q * Hkv * n_hc * n_split;
-  const int64_t nwarps = (int64_t)gridDim.x * kAWarps;
-  for (int64_t item = (int64_t)blockIdx.x * kAWarps + warp; item < items; item += nwarps) {
+  const int64_t nwarps = (int64_t)gridDim.x * DecodeShape::kWarps;
+  for (int64_t item = (int64_t)blockIdx.x * DecodeShape::kWarps + warp; item < items; item += nwarps) {
     const int split = (int)(item % n_split);
     const int64_t wi = item / n_split;          // (row, g, hc)
     const int hc = (int)(wi % n_hc);
@@ -451,7 +465,7 @@ sparse_attn_decode_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat
       const __nv_bfloat16* kh = k + (bb * Hkv + g) * L_cap * kHeadDim;
       const __nv_bfloat16* vh = v + (bb * Hkv + g) * L_cap * kHeadDim;
       float o[8][4], m2[2], l[2];
-      attend_slots(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end, scale * kLog2e, ring, ids, o,
+      attend_slots<DecodeShape::kRing>(q + (row * Hq + qh0) * kHeadDim, n_heads, kh, vh, a, r, s_beg, s_end, scale * kLog2e, ring, ids, o,
                    m2, l);
       float* st = reinterpret_cast<float*>(wbuf);
       stage_o(st, o, 1.f, 1.f);
@@ -506,13 +520,13 @@ size_t decode_workspace_bytes(int64_t B, int Hq, int Hkv, int k_b, int r) {
 
 // Grid of a persistent attention kernel (<= one CTA per SM); raises the
 // kernel's dynamic shared memory limit on the current device first.
-static cudaError_t attn_grid(const void* kernel, int64_t items, int* grid) {
-  cudaError_t e = ensure_dyn_smem(kernel, kASmemBytes);
+static cudaError_t attn_grid(const void* kernel, int smem_bytes, int warps, int64_t items, int* grid) {
+  cudaError_t e = ensure_dyn_smem(kernel, smem_bytes);
   if (e != cudaSuccess) return e;
   int sms = 0;
   e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
-  const int64_t need = (items + kAWarps - 1) / kAWarps;
+  const int64_t need = (items + warps - 1) / warps;
   *grid = (int)(need < sms ? need : sms);
   return cudaSuccess;
 }
@@ -526,9 +540,10 @@ cudaError_t launch_sparse_attn_prefill(const __nv_bfloat16* q, const __nv_bfloat
   const int64_t items = B * n_q * Hkv * n_hc;
   if (items == 0) return cudaSuccess;
   int grid = 0;
-  cudaError_t e = attn_grid(reinterpret_cast<const void*>(sparse_attn_prefill_kernel), items, &grid);
+  cudaError_t e = attn_grid(reinterpret_cast<const void*>(sparse_attn_prefill_kernel), PrefillShape::kSmemBytes,
+                            PrefillShape::kWarps, items, &grid);
   if (e != cudaSuccess) return e;
-  sparse_attn_prefill_kernel<<<grid, kAWarps * 32, kASmemBytes, st>>>(q, k, v, L_cap, q_pos, idx, count, B, n_q,
+  sparse_attn_prefill_kernel<<<grid, PrefillShape::kWarps * 32, PrefillShape::kSmemBytes, st>>>(q, k, v, L_cap, q_pos, idx, count, B, n_q,
                                                                     Hq, Hkv, r, k_b, scale, out, lse);
   return count_launch(cudaGetLastError());
 }
@@ -554,21 +569,23 @@ cudaError_t launch_sparse_attn_decode(const __nv_bfloat16* q, const __nv_bfloat1
   // As many splits per unit as fill the resident warps once (at least one,
   // at most max_split), each a whole number of 16-slot groups.
   int grid = 0;
-  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), units * max_split, &grid);
+  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), DecodeShape::kSmemBytes,
+                DecodeShape::kWarps, units * max_split, &grid);
   if (e != cudaSuccess) return e;
   int sms = 0;
   e = current_sm_count(&sms);
   if (e != cudaSuccess) return e;
-  int64_t n_split = (int64_t)sms * kAWarps / units;
+  int64_t n_split = (int64_t)sms * DecodeShape::kWarps / units;
   n_split = n_split < 1 ? 1 : (n_split > max_split ? max_split : n_split);
   const int max_tok = k_b * r + r - 1;
   int split_len = (int)((max_tok + n_split - 1) / n_split);
   split_len = (split_len + kAGroup - 1) / kAGroup * kAGroup;
   n_split = (max_tok + split_len - 1) / split_len;
-  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), units * n_split, &grid);
+  e = attn_grid(reinterpret_cast<const void*>(sparse_attn_decode_kernel), DecodeShape::kSmemBytes,
+                DecodeShape::kWarps, units * n_split, &grid);
   if (e != cudaSuccess) return e;
-  return count_launch(launch_dependent(sparse_attn_decode_kernel, dim3((unsigned)grid), dim3(kAWarps * 32),
-                                      (size_t)kASmemBytes, st, q, k, v, L_cap, cache_len, idx, count, B, n_q, Hq, Hkv,
+  return count_launch(launch_dependent(sparse_attn_decode_kernel, dim3((unsigned)grid),
+                                      dim3(DecodeShape::kWarps * 32), (size_t)DecodeShape::kSmemBytes, st, q, k, v, L_cap, cache_len, idx, count, B, n_q, Hq, Hkv,
                                       r, k_b, (int)n_split, split_len, scale, part_o, part_ml, unit_done, out, lse));
 }
 
