@@ -47,6 +47,10 @@ qsa_status check_config(const qsa_config* c) {
 
 int k_blocks(const qsa_config* c) { return (c->k_tokens + c->r - 1) / c->r; }
 
+// Longest K/V buffer the attention kernels take: they index its tokens with
+// 32-bit integers.
+constexpr int64_t kMaxLCap = 0x7fffffff;
+
 // Softmax scale of the attention calls: a caller value <= 0 selects the usual
 // 1 / sqrt(head_dim).
 float softmax_scale(const qsa_config* c, float scale) {
@@ -222,7 +226,7 @@ qsa_status qsa_sparse_attn_prefill_impl(const qsa_config* cfg, const void* q, co
   if (s != QSA_OK) return s;
   if (B < 0 || n_q < 0 || L_cap < 0 || Hq < 1 || Hkv < 1 || !std::isfinite(scale)) return QSA_ERR_INVALID_ARG;
   if (impl != QSA_ATTN_AUTO && impl != QSA_ATTN_TCGEN05 && impl != QSA_ATTN_MMA_SYNC) return QSA_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0) return QSA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0 || L_cap > kMaxLCap) return QSA_ERR_UNSUPPORTED;
   const bool tc_ok = tc_attention_supported(Hq, Hkv, cfg->r);
   if (impl == QSA_ATTN_TCGEN05 && !tc_ok) return QSA_ERR_UNSUPPORTED;
   if (B == 0 || n_q == 0) return QSA_OK;
@@ -265,7 +269,7 @@ qsa_status qsa_sparse_attn_decode(const qsa_config* cfg, const void* q, const vo
   qsa_status s = check_config(cfg);
   if (s != QSA_OK) return s;
   if (B < 0 || L_cap < 0 || Hq < 1 || Hkv < 1 || !std::isfinite(scale)) return QSA_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0) return QSA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0 || L_cap > kMaxLCap) return QSA_ERR_UNSUPPORTED;
   if (B == 0) return QSA_OK;
   if (!q || !k_cache || !v_cache || !cache_len || !idx || !count || !out || L_cap < 1)
     return QSA_ERR_INVALID_ARG;
@@ -294,7 +298,7 @@ qsa_status qsa_sparse_attn_decode_multi(const qsa_config* cfg, const void* q, co
   qsa_status s = check_config(cfg);
   if (s != QSA_OK) return s;
   if (B < 0 || n_q < 1 || L_cap < 0 || Hq < 1 || Hkv < 1 || !std::isfinite(scale)) return QSA_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0) return QSA_ERR_UNSUPPORTED;
+  if (Hq % Hkv != 0 || L_cap > kMaxLCap) return QSA_ERR_UNSUPPORTED;
   if (B == 0) return QSA_OK;
   if (!q || !k_cache || !v_cache || !cache_len || !idx || !count || !out || L_cap < 1)
     return QSA_ERR_INVALID_ARG;

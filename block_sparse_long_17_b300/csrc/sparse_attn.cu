@@ -149,15 +149,15 @@ __device__ __forceinline__ void issue_stage(uint32_t kst, const AttnRow& a, int 
   const int lane = threadIdx.x & 31;
   int slot = s0 + (lane & 15);
   if (slot >= slot_end) slot = slot_end - 1;
-  const int64_t my_tok = slot_token_window(a, r, slot, ids, w0);  // token of row lane % 16
+  const int my_tok = (int)slot_token_window(a, r, slot, ids, w0);  // token of row lane % 16 (L_cap < 2^31)
   const int chunk = lane & 15, sub = lane >> 4;
   const uint32_t vst = kst + kAGroup * 256;
 #pragma unroll
   for (int j = 0; j < kAGroup / 2; ++j) {
     const int row = 2 * j + sub;
-    const int64_t tok = __shfl_sync(0xffffffffu, my_tok, row);
-    cp_async16(kst + swz(row, chunk), reinterpret_cast<const char*>(kh + tok * kHeadDim) + chunk * 16);
-    cp_async16(vst + swz(row, chunk), reinterpret_cast<const char*>(vh + tok * kHeadDim) + chunk * 16);
+    const int tok = __shfl_sync(0xffffffffu, my_tok, row);
+    cp_async16(kst + swz(row, chunk), reinterpret_cast<const char*>(kh + (int64_t)tok * kHeadDim) + chunk * 16);
+    cp_async16(vst + swz(row, chunk), reinterpret_cast<const char*>(vh + (int64_t)tok * kHeadDim) + chunk * 16);
   }
 }
 

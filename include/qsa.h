@@ -180,6 +180,9 @@ qsa_status qsa_index_topk_fallback_rows(const qsa_config* cfg, int64_t B, int64_
  *   lse[h]= log sum_{t in T_i} exp(scale * <q[h], k[g, t]>).
  *   q      bf16 [B][n_q][Hq][head_dim]   (already position-encoded by the caller)
  *   k, v   bf16 [B][Hkv][L_cap][head_dim]; every token of T_i must be < L_cap.
+ *          L_cap above 2^31 - 1 returns QSA_ERR_UNSUPPORTED (the kernels index
+ *          tokens with 32-bit integers); the same holds for every attention
+ *          call below.
  *   q_pos  device int64 [B] as for qsa_index_topk (chunked prefill = q_pos > 0).
  *   idx, count  as written by qsa_index_topk.
  *   scale  softmax scale; a value <= 0 selects 1 / sqrt(head_dim).  Not finite:

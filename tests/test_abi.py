@@ -95,6 +95,14 @@ def test_null_and_negative_arguments(lib):
     # misaligned tensor pointer
     odd = ctypes.c_void_p(258)
     assert lib.qsa_compress_keys(ctypes.byref(c), odd, 0, 1, 0, 1, fake, 0, None) == 1
+    # K/V buffers longer than 32-bit token indices reach
+    big = 1 << 31
+    assert lib.qsa_sparse_attn_prefill(ctypes.byref(c), fake, fake, fake, big, fake, fake, fake, 1, 1,
+                                       16, 2, 0.1, fake, None, None) == 2
+    assert lib.qsa_sparse_attn_decode(ctypes.byref(c), fake, fake, fake, big, fake, fake, fake, 1, 16, 2, 0.1,
+                                      fake, None, fake, 1 << 30, None) == 2
+    assert lib.qsa_sparse_attn_decode_multi(ctypes.byref(c), fake, fake, fake, big, fake, fake, fake, 1, 2, 16, 2,
+                                            0.1, fake, None, fake, 1 << 30, None) == 2
 
 
 def test_workspace_sizes_and_checks(lib):
