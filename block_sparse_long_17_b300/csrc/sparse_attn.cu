@@ -24,9 +24,11 @@
 //     shared-memory read rather than after an L2 round trip;
 //   * block and slot arithmetic uses shifts (r is a power of two);
 //   * S^T = K Q^T (m16n8k16 MMAs, 16 tokens x 8 heads, K fragments by
-//     ldmatrix) runs its 8 k-steps as two accumulator chains of 4, summed.
-// Then an fp32 online softmax per head, and O^T += V^T P^T (V fragments by
-// ldmatrix.trans, P transposed by movmatrix).
+//     ldmatrix) runs its 8 k-steps as two accumulator chains of 4, summed;
+//   * the fp32 online softmax and the rescaling of O use packed fp32x2 adds,
+//     multiplies and fmas on the lane's two heads (the same roundings).
+// Then O^T += V^T P^T (V fragments by ldmatrix.trans, P transposed by
+// movmatrix).
 #include "common.cuh"
 
 namespace qsa {
@@ -234,13 +236,19 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
       mma_bf16_16816(sc, af, qf[ks]);
       mma_bf16_16816(sd, ag, qf[ks + 1]);
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sc[e] += sd[e];
+    {
+      const float2 s01 = __fadd2_rn(make_float2(sc[0], sc[1]), make_float2(sd[0], sd[1]));
+      const float2 s23 = __fadd2_rn(make_float2(sc[2], sc[3]), make_float2(sd[2], sd[3]));
+      sc[0] = s01.x; sc[1] = s01.y; sc[2] = s23.x; sc[3] = s23.y;
+    }
     // sc: (slot s0+gid, head 2t), (s0+gid, 2t+1), (s0+gid+8, 2t), (s0+gid+8, 2t+1)
-    const float x0 = va_ok ? sc[0] * scale_log2 : -INFINITY;
-    const float x1 = va_ok ? sc[1] * scale_log2 : -INFINITY;
-    const float x2 = vb_ok ? sc[2] * scale_log2 : -INFINITY;
-    const float x3 = vb_ok ? sc[3] * scale_log2 : -INFINITY;
+    const float2 sl = make_float2(scale_log2, scale_log2);
+    const float2 y01 = __fmul2_rn(make_float2(sc[0], sc[1]), sl);
+    const float2 y23 = __fmul2_rn(make_float2(sc[2], sc[3]), sl);
+    const float x0 = va_ok ? y01.x : -INFINITY;
+    const float x1 = va_ok ? y01.y : -INFINITY;
+    const float x2 = vb_ok ? y23.x : -INFINITY;
+    const float x3 = vb_ok ? y23.y : -INFINITY;
     float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -249,17 +257,27 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
     }
     // Slot s0 is always valid, so the new maxima are finite.
     const float mn0 = fmaxf(mrun0, mx0), mn1 = fmaxf(mrun1, mx1);
-    const float al0 = exp2f(mrun0 - mn0), al1 = exp2f(mrun1 - mn1);
+    const float2 nmn = make_float2(-mn0, -mn1);
+    const float2 da = __fadd2_rn(make_float2(mrun0, mrun1), nmn);
+    const float al0 = exp2f(da.x), al1 = exp2f(da.y);
     mrun0 = mn0;
     mrun1 = mn1;
-    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-    l0 = l0 * al0 + p0 + p2;
-    l1 = l1 * al1 + p1 + p3;
+    const float2 d01 = __fadd2_rn(make_float2(x0, x1), nmn);
+    const float2 d23 = __fadd2_rn(make_float2(x2, x3), nmn);
+    const float p0 = exp2f(d01.x), p1 = exp2f(d01.y);
+    const float p2 = exp2f(d23.x), p3 = exp2f(d23.y);
+    {
+      const float2 lf = __fadd2_rn(__ffma2_rn(make_float2(l0, l1), make_float2(al0, al1), make_float2(p0, p1)),
+                                   make_float2(p2, p3));
+      l0 = lf.x;
+      l1 = lf.y;
+    }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] *= al0; o[mt][2] *= al0;
-      o[mt][1] *= al1; o[mt][3] *= al1;
+      const float2 al = make_float2(al0, al1);
+      const float2 u = __fmul2_rn(make_float2(o[mt][0], o[mt][1]), al);
+      const float2 w = __fmul2_rn(make_float2(o[mt][2], o[mt][3]), al);
+      o[mt][0] = u.x; o[mt][1] = u.y; o[mt][2] = w.x; o[mt][3] = w.y;
     }
     // P^T as the B operand: transpose the (slot x head) tiles.
     const uint32_t pb[2] = {movmatrix_trans(pack_bf16x2(p0, p1)), movmatrix_trans(pack_bf16x2(p2, p3))};
