@@ -478,12 +478,17 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         tma_load_2d(S.b[0], &tm_q, &S.b_full, 0, qrow);
         tma_load_2d(S.b[1], &tm_q, &S.b_full, 64, qrow);
         const int total = m.npilot + m.nchunks;
+        int pph = 0, pkc = 0;  // phase and column of the next pilot chunk
         for (int x = 0; x < total; ++x, ++it) {
           const int st = it % kAStages;
           if (!mbar_wait(&S.a_empty[st], ((it / kAStages) & 1) ^ 1, abort_flag, kWaitCycles, 64)) { ok = false; break; }
           mbar_arrive_expect_tx(&S.a_full[st], kABytes);
           if (x < m.npilot) {  // blocks 16 (kMB kc + row) + ph
-            const int ph = x / m.mc, kc = x % m.mc;
+            const int ph = pph, kc = pkc;
+            if (++pkc == m.mc) {
+              pkc = 0;
+              ++pph;
+            }
             tma_load_4d(S.a[st][0], &tm_kp, &S.a_full[st], 0, ph, kc * kMB, (int)m.bb);
             tma_load_4d(S.a[st][1], &tm_kp, &S.a_full[st], 64, ph, kc * kMB, (int)m.bb);
           } else {
@@ -570,6 +575,7 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         cntw[k2] = 0;
       }
       const int total = m.npilot + m.nchunks;
+      int pph = 0, pkc = 0;  // phase and column of the next pilot chunk
       for (int x = 0; x < total; ++x, ++ct) {
         const bool pilot = x < m.npilot;
         if (x == m.npilot) {
@@ -666,8 +672,12 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         // Blocks of this warp's lanes: main chunk ch holds blocks gbase + lane,
         // gbase = q4 R + 32 ch (the quarter's own region of R = 32 nchunks
         // blocks); pilot chunks hold blocks 16 (gbase + lane) + ph, gbase = kMB kc + 32 q4.
-        const int ph = pilot ? x / m.mc : 0;
-        const int gbase = pilot ? (x % m.mc) * kMB + 32 * q4 : q4 * (m.nchunks * 32) + (x - m.npilot) * 32;
+        const int ph = pilot ? pph : 0;
+        const int gbase = pilot ? pkc * kMB + 32 * q4 : q4 * (m.nchunks * 32) + (x - m.npilot) * 32;
+        if (pilot && ++pkc == m.mc) {  // pilot chunk x is phase x / mc, column x % mc
+          pkc = 0;
+          ++pph;
+        }
         const int bi = pilot ? (gbase + lane) * kPilotStride + ph : gbase + lane;
         // Every block of the warp is visible to all its tokens when they end
         // below the first token's visible range.
@@ -748,21 +758,24 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 // exact top-k_B of the entries their tile collected (finalize_row), or are
 // queued for the exact fallback kernel when their buffer fell outside
 // [k_B, kFCap] entries or a segment overflowed.
+template <int TT>
 __global__ void __launch_bounds__(32 * kFinKWarps, 4)
 index_finalize_kernel(const uint2* __restrict__ buf, const int* __restrict__ cnt, const int64_t* __restrict__ q_pos,
-                      int64_t n_q, int64_t tiles_per_seq, int64_t t_begin, int64_t t_count, int rshift, int k_b,
-                      int64_t c_cap, int tt, int32_t* __restrict__ idx, int32_t* __restrict__ count,
+                      int64_t n_q, int tiles_per_seq, int t_begin, int t_count, int rshift, int k_b,
+                      int64_t c_cap, int32_t* __restrict__ idx, int32_t* __restrict__ count,
                       int64_t* __restrict__ fb_rows, int* __restrict__ fb_count) {
+  constexpr int tt = TT;
   __shared__ __align__(16) uint32_t hist[kFinKWarps][512];
   __shared__ int32_t ids[kFinKWarps][kFCap];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t rows = t_count * tt;  // tt: tokens per tile
-  for (int64_t rr = (int64_t)blockIdx.x * kFinKWarps + w; rr < rows; rr += (int64_t)gridDim.x * kFinKWarps) {
-    const int64_t lt = rr / tt;
-    const int t = (int)(rr % tt);
-    const int64_t tile = t_begin + lt;
-    const int64_t bb = tile / tiles_per_seq;
-    const int64_t tok = (tile % tiles_per_seq) * tt + t;
+  const int rows = t_count * tt;  // tt: tokens per tile; 32-bit row and tile indices
+  for (int rr = blockIdx.x * kFinKWarps + w; rr < rows; rr += gridDim.x * kFinKWarps) {
+    const int lt = rr / tt;
+    const int t = rr - lt * tt;
+    const int tile = t_begin + lt;
+    const int bbi = tile / tiles_per_seq;
+    const int64_t bb = bbi;
+    const int64_t tok = (int64_t)(tile - bbi * tiles_per_seq) * tt + t;
     if (tok >= n_q) continue;
     int64_t c = (q_pos[bb] + tok + 1) >> rshift;
     if (c > c_cap) c = c_cap;
@@ -910,6 +923,7 @@ cudaError_t launch_index_fused(int H, const __nv_bfloat16* qt, const __nv_bfloat
   const int tt = fused_tile_tokens(H);
   const int aim = pilot_aim(k_b);
   if (L.n_tiles == 0) return cudaSuccess;
+  if (L.n_tiles > 0x7fffffff) return cudaErrorInvalidValue;  // the finalize indexes tiles with 32 bits
   PFN_cuTensorMapEncodeTiled_v12000 encode = get_encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   char* w = static_cast<char*>(ws);
@@ -992,9 +1006,15 @@ cudaError_t launch_index_fused(int H, const __nv_bfloat16* qt, const __nv_bfloat
     e = count_launch(cudaGetLastError());
     if (e != cudaSuccess) return e;
     const int64_t fin_blocks = (t_count * tt + kFinKWarps - 1) / kFinKWarps;
-    index_finalize_kernel<<<(unsigned)fin_blocks, 32 * kFinKWarps, 0, st>>>(
-        buf, cnt, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, n_blocks_max, tt, idx, count, fb_rows,
-        fb_count);
+    // Tile and row indices of a launch fit 32 bits (at most kTilesPerLaunch tiles).
+    if (tt == 48)
+      index_finalize_kernel<48><<<(unsigned)fin_blocks, 32 * kFinKWarps, 0, st>>>(
+          buf, cnt, q_pos, n_q, (int)L.tiles_per_seq, (int)t_begin, (int)t_count, rshift, k_b, n_blocks_max, idx,
+          count, fb_rows, fb_count);
+    else
+      index_finalize_kernel<24><<<(unsigned)fin_blocks, 32 * kFinKWarps, 0, st>>>(
+          buf, cnt, q_pos, n_q, (int)L.tiles_per_seq, (int)t_begin, (int)t_count, rshift, k_b, n_blocks_max, idx,
+          count, fb_rows, fb_count);
     e = count_launch(cudaGetLastError());
     if (e != cudaSuccess) return e;
   }
