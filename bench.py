@@ -758,7 +758,8 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev) -> 
     chunks of e2e_chunk_bounds: one stream copies chunk i in, one computes it
     (compress its blocks, select and attend its rows against the prefix), one
     copies its output back, so that the copies of one chunk overlap the kernels
-    of another.  The decode step follows on the compute stream."""
+    of another.  The decode step runs first on the compute stream, while the
+    first chunk's inputs come in."""
     import torch
     host_in = {k: wl[k].cpu().pin_memory() for k in ("q_idx", "k_idx", "q", "k", "v")}
     dev_in = {k: torch.empty_like(wl[k]) for k in host_in}
@@ -788,6 +789,21 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev) -> 
         with torch.cuda.stream(s_in):
             dq_d.copy_(dq_h, non_blocking=True)
             dqi_d.copy_(dqi_h, non_blocking=True)
+            dec_in = torch.cuda.Event()
+            dec_in.record(s_in)
+        # The decode step needs none of the prefill: it runs first, while the
+        # first chunk's inputs are still coming in.
+        s_cmp.wait_event(dec_in)
+        q_pos = dwl["cache_lens"] - 1
+        qsa.qsa_index_topk(dcfg, dqi_d, dwl["kbar"], q_pos, dwl["n_blocks"], dec.idx, dec.count, dec.ws_idx,
+                           stream=s_cmp)
+        qsa.qsa_sparse_attn_decode(dcfg, dq_d, dwl["k"], dwl["v"], dwl["cache_lens"], dec.idx.view(dspec.batch, -1),
+                                   dec.count.view(dspec.batch), dec.out, dec.ws_attn, dec.lse, stream=s_cmp)
+        done = torch.cuda.Event()
+        done.record(s_cmp)
+        s_out.wait_event(done)
+        with torch.cuda.stream(s_out):
+            dout_h.copy_(dec.out, non_blocking=True)
         for i, (lo, hi) in enumerate(chunks):
             with torch.cuda.stream(s_in):
                 for key in ("k_idx", "q_idx", "q"):
@@ -810,16 +826,6 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev) -> 
             s_out.wait_event(done)
             with torch.cuda.stream(s_out):
                 out_h[:, lo:hi].copy_(pre.out[:, lo:hi], non_blocking=True)
-        q_pos = dwl["cache_lens"] - 1
-        qsa.qsa_index_topk(dcfg, dqi_d, dwl["kbar"], q_pos, dwl["n_blocks"], dec.idx, dec.count, dec.ws_idx,
-                           stream=s_cmp)
-        qsa.qsa_sparse_attn_decode(dcfg, dq_d, dwl["k"], dwl["v"], dwl["cache_lens"], dec.idx.view(dspec.batch, -1),
-                                   dec.count.view(dspec.batch), dec.out, dec.ws_attn, dec.lse, stream=s_cmp)
-        done = torch.cuda.Event()
-        done.record(s_cmp)
-        s_out.wait_event(done)
-        with torch.cuda.stream(s_out):
-            dout_h.copy_(dec.out, non_blocking=True)
         for s in (s_in, s_cmp, s_out):
             fin = torch.cuda.Event()
             fin.record(s)
