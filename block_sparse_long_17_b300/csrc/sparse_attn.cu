@@ -25,8 +25,11 @@
 //   * block and slot arithmetic uses shifts (r is a power of two);
 //   * S^T = K Q^T (m16n8k16 MMAs, 16 tokens x 8 heads, K fragments by
 //     ldmatrix) runs its 8 k-steps as two accumulator chains of 4, summed;
-//   * the fp32 online softmax and the rescaling of O use packed fp32x2 adds,
-//     multiplies and fmas on the lane's two heads (the same roundings).
+//   * the fp32 online softmax keeps its running maximum until a score exceeds
+//     it by more than 8 (log2 units); only then are the maximum reduced across
+//     lanes and O and l rescaled (P stays below 2^8, so fp32 sums and the bf16
+//     P are safe).  Its arithmetic uses packed fp32x2 adds, multiplies and
+//     fmas on the lane's two heads.
 // Then O^T += V^T P^T (V fragments by ldmatrix.trans, P transposed by
 // movmatrix).
 #include "common.cuh"
@@ -249,35 +252,44 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
     const float x1 = va_ok ? y01.y : -INFINITY;
     const float x2 = vb_ok ? y23.x : -INFINITY;
     const float x3 = vb_ok ? y23.y : -INFINITY;
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+    // Lazy running maximum: the stage keeps mrun unless one of its scores
+    // exceeds it by more than 8 (log2 units); then the maximum is reduced
+    // across the head's lanes and O, l are rescaled.  Otherwise P = 2^(x - mrun)
+    // <= 2^8, and O / l and mrun + log2 l are unchanged in exact arithmetic.
+    float2 al = make_float2(1.f, 1.f);
+    {
+      const float t0 = mrun0 + 8.f, t1 = mrun1 + 8.f;
+      const bool big = x0 > t0 || x2 > t0 || x1 > t1 || x3 > t1;
+      if (__any_sync(0xffffffffu, big)) {
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        // Slot s0 is always valid, so the new maxima are finite.
+        const float mn0 = fmaxf(mrun0, mx0), mn1 = fmaxf(mrun1, mx1);
+        const float2 da = __fadd2_rn(make_float2(mrun0, mrun1), make_float2(-mn0, -mn1));
+        al = make_float2(exp2f(da.x), exp2f(da.y));
+        mrun0 = mn0;
+        mrun1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const float2 u = __fmul2_rn(make_float2(o[mt][0], o[mt][1]), al);
+          const float2 w = __fmul2_rn(make_float2(o[mt][2], o[mt][3]), al);
+          o[mt][0] = u.x; o[mt][1] = u.y; o[mt][2] = w.x; o[mt][3] = w.y;
+        }
+      }
     }
-    // Slot s0 is always valid, so the new maxima are finite.
-    const float mn0 = fmaxf(mrun0, mx0), mn1 = fmaxf(mrun1, mx1);
-    const float2 nmn = make_float2(-mn0, -mn1);
-    const float2 da = __fadd2_rn(make_float2(mrun0, mrun1), nmn);
-    const float al0 = exp2f(da.x), al1 = exp2f(da.y);
-    mrun0 = mn0;
-    mrun1 = mn1;
+    const float2 nmn = make_float2(-mrun0, -mrun1);
     const float2 d01 = __fadd2_rn(make_float2(x0, x1), nmn);
     const float2 d23 = __fadd2_rn(make_float2(x2, x3), nmn);
     const float p0 = exp2f(d01.x), p1 = exp2f(d01.y);
     const float p2 = exp2f(d23.x), p3 = exp2f(d23.y);
     {
-      const float2 lf = __fadd2_rn(__ffma2_rn(make_float2(l0, l1), make_float2(al0, al1), make_float2(p0, p1)),
-                                   make_float2(p2, p3));
+      const float2 lf = __fadd2_rn(__ffma2_rn(make_float2(l0, l1), al, make_float2(p0, p1)), make_float2(p2, p3));
       l0 = lf.x;
       l1 = lf.y;
-    }
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const float2 al = make_float2(al0, al1);
-      const float2 u = __fmul2_rn(make_float2(o[mt][0], o[mt][1]), al);
-      const float2 w = __fmul2_rn(make_float2(o[mt][2], o[mt][3]), al);
-      o[mt][0] = u.x; o[mt][1] = u.y; o[mt][2] = w.x; o[mt][3] = w.y;
     }
     // P^T as the B operand: transpose the (slot x head) tiles.
     const uint32_t pb[2] = {movmatrix_trans(pack_bf16x2(p0, p1)), movmatrix_trans(pack_bf16x2(p2, p3))};
