@@ -248,10 +248,13 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
     const float2 sl = make_float2(scale_log2, scale_log2);
     const float2 y01 = __fmul2_rn(make_float2(sc[0], sc[1]), sl);
     const float2 y23 = __fmul2_rn(make_float2(sc[2], sc[3]), sl);
-    const float x0 = va_ok ? y01.x : -INFINITY;
-    const float x1 = va_ok ? y01.y : -INFINITY;
-    const float x2 = vb_ok ? y23.x : -INFINITY;
-    const float x3 = vb_ok ? y23.y : -INFINITY;
+    float x0 = y01.x, x1 = y01.y, x2 = y23.x, x3 = y23.y;
+    if (s0 + kAGroup > slot_end) {  // the item's last stage: slots past slot_end are masked
+      x0 = va_ok ? x0 : -INFINITY;
+      x1 = va_ok ? x1 : -INFINITY;
+      x2 = vb_ok ? x2 : -INFINITY;
+      x3 = vb_ok ? x3 : -INFINITY;
+    }
     // Lazy running maximum: the stage keeps mrun unless one of its scores
     // exceeds it by more than 8 (log2 units); then the maximum is reduced
     // across the head's lanes and O, l are rescaled.  Otherwise P = 2^(x - mrun)
