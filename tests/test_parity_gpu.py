@@ -218,6 +218,40 @@ def test_dense_limit_equals_torch_sdpa():
     assert np.abs(gpu["out"][0] - ref.cpu().numpy()).max() <= QC.OUT_ATOL
 
 
+def test_attention_rescales_when_later_scores_jump():
+    """The online softmax keeps its running maximum until a score exceeds it by
+    more than 8 (log2 units) and only then rescales O and the sum.  The
+    attention keys of the sequence's second half are scaled by 12, so that a
+    row's scores jump far above its running maximum once its token set (the
+    selected blocks in ascending order, then the tail) reaches them; the rows
+    are checked against the oracle, and the same rows with the keys unscaled
+    exercise the path that never rescales after its first stage."""
+    spec, wl = small_case(2048, 512, seed=21)
+    cfg = cfg_for(spec)
+    rows = [1030, 1100, 1500, 1777, 2000, 2047]
+    for factor in (12.0, 1.0):
+        k = wl["k"].float()
+        k[:, :, 1024:] *= factor
+        w = {**wl, "k": k.to(torch.bfloat16)}
+        gpu = run_prefill(cfg, w)
+        res = QC.oracle_rows(w, rows, cfg=cfg)
+        # Selections as everywhere (the indexer keys are unchanged) ...
+        st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], None, None, cfg.k_b, cfg.r)
+        assert st["exact"] == len(rows), st
+        # ... outputs within the bound of the kernel's two bf16 roundings: P for
+        # the PV product (2^-9 of each weight, so at most 2^-9 max|v| in o) and
+        # o itself (half an ulp, 2^-9 |o| <= 2^-9 max|v|).  With the keys scaled
+        # a row's softmax is dominated by a token or two and |o| nears max|v|,
+        # beyond the fixed tolerance meant for averaging softmaxes.
+        v = QC.bf16_to_np32(w["v"][0]).astype(np.float64)
+        for n, j in enumerate(rows):
+            toks = O.token_set(j, gpu["idx"][0][j][:int(gpu["count"][0][j])].astype(np.int64), cfg.r)
+            vmax = np.abs(v[:, toks]).max()
+            err = np.abs(gpu["out"][0][j] - res["out"][n]).max()
+            assert err <= 2.0 ** -8 * vmax + 1e-4, (factor, j, err, vmax)
+            assert np.abs(gpu["lse"][0][j] - res["lse"][n]).max() <= 1e-3 * max(1.0, factor)
+
+
 def test_exact_ties_take_lowest_block_ids():
     """All-zero indexer keys: every score is 0, so the first k_B blocks win."""
     spec, wl = small_case(300, 64)
