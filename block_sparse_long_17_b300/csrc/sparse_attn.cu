@@ -23,6 +23,8 @@
 //     blocks, ids checked there), so a stage's copies are issued after a
 //     shared-memory read rather than after an L2 round trip;
 //   * block and slot arithmetic uses shifts (r is a power of two);
+//   * the streamed q rows, block ids and outputs are loaded and stored with
+//     evict-first hints, so that L2 keeps the gathered K/V rows instead;
 //   * S^T = K Q^T (m16n8k16 MMAs, 16 tokens x 8 heads, K fragments by
 //     ldmatrix) runs its 8 k-steps as two accumulator chains of 4, summed;
 //   * the fp32 online softmax keeps its running maximum until a score exceeds
@@ -77,7 +79,7 @@ __device__ __forceinline__ void load_id_window(int32_t* ids, const AttnRow& a, i
 #pragma unroll
   for (int j = 0; j < kAIds / 32; ++j) {
     const int b = w0 + lane + 32 * j;
-    v[j] = b < a.cnt ? __ldg(a.sel + b) : 0;
+    v[j] = b < a.cnt ? __ldcs(a.sel + b) : 0;
   }
 #pragma unroll
   for (int j = 0; j < kAIds / 32; ++j) {
@@ -207,8 +209,8 @@ __device__ __forceinline__ void attend_slots(const __nv_bfloat16* __restrict__ q
     const uint32_t* qrow = reinterpret_cast<const uint32_t*>(q_heads + gid * kHeadDim);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      qf[ks][0] = gid < n_heads ? __ldg(qrow + 8 * ks + t) : 0u;
-      qf[ks][1] = gid < n_heads ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+      qf[ks][0] = gid < n_heads ? __ldcs(qrow + 8 * ks + t) : 0u;
+      qf[ks][1] = gid < n_heads ? __ldcs(qrow + 8 * ks + 4 + t) : 0u;
     }
   }
 #pragma unroll
@@ -374,7 +376,7 @@ sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
       const float* srow = st + h * kHeadDim;
       const int d = 4 * lane;
       const uint2 pk = make_uint2(pack_bf16x2(srow[d], srow[d + 1]), pack_bf16x2(srow[d + 2], srow[d + 3]));
-      *reinterpret_cast<uint2*>(out + ((row * Hq) + qh0 + h) * kHeadDim + d) = pk;
+      __stcs(reinterpret_cast<uint2*>(out + ((row * Hq) + qh0 + h) * kHeadDim + d), pk);
     }
     if (lse != nullptr && gid == 0) {
       // natural-log LSE = (m2 + log2 l) * ln 2
