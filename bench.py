@@ -55,7 +55,7 @@ def job_tokens_per_s(world: int, tokens_per_rank: int, prefill_ms: float) -> flo
 #       -k "regex:sparse_attn_prefill" -c 1 python bench.py --decode-workload none
 #       --multi-decode-workload none --no-extras --steps 1 --warmup 3 --no-cpu-baseline --no-e2e
 # A kernel or workload not listed (or a kernel changed since the capture) reports null.
-MEASURED_TRAFFIC = {("attn_prefill", "drift_prefill_128k"): 2237968896 + 545587712}
+MEASURED_TRAFFIC = {("attn_prefill", "drift_prefill_128k"): 2054448384 + 544514048}
 
 
 def peaks():
