@@ -29,7 +29,7 @@
 //     ldmatrix) runs its 8 k-steps as two accumulator chains of 4, summed;
 //   * the fp32 online softmax keeps its running maximum until a score exceeds
 //     it by more than 8 (log2 units); only then are the maximum reduced across
-//     lanes and O and l rescaled (P stays below 2^8, so fp32 sums and the bf16
+//     lanes and O and l rescaled (P stays at or below 2^8, so fp32 sums and the bf16
 //     P are safe).  Its arithmetic uses packed fp32x2 adds, multiplies and
 //     fmas on the lane's two heads.
 // Then O^T += V^T P^T (V fragments by ldmatrix.trans, P transposed by
