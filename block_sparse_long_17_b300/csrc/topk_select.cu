@@ -205,8 +205,8 @@ cudaError_t launch_topk_select(const float* S, int64_t s_stride, const int64_t* 
 
 
 // ---------------------------------------------------------------------------------------------
-// Two-pass selection for long rows: one pass for the histogram of the top 11
-// bits, one ordered pass that copies every entry at or above the boundary bin
+// Two-pass selection for long rows: one pass for a histogram of 1/32-octave
+// bins (first_bin, below), one ordered pass that copies every entry at or above the boundary bin
 // into shared memory (at most kSelCand entries, in block order); the remaining
 // refinement and the emission run on that copy.  Rows whose boundary bin is
 // too full fall back to cta_select_row.
@@ -308,10 +308,31 @@ __device__ void select_from_candidates(SelectFastSmem& sm, int ncand, uint32_t l
 // ---------------------------------------------------------------------------------------------
 // The same selection with each row split over a cluster of kSelCluster CTAs
 // (decode: few rows, long rows).  Every CTA takes a share of the row: local
-// histograms of the top 11 bits, merged by every CTA through distributed
-// shared memory; ordered copies of the entries at or above the boundary bin,
-// gathered into the first CTA's candidate arrays in rank (= block) order; that
-// CTA refines and emits.
+// histograms of 1/32-octave bins (first_bin), merged by the first CTA through
+// distributed shared memory; ordered copies of the entries at or above the
+// boundary bin, gathered into the first CTA's candidate arrays in rank (=
+// block) order; that CTA refines and emits.
+//
+// First-pass bins: 32 per octave of the fp32 score over the 64 octaves
+// [2^-30, 2^34), clamped at both ends (bin 0 also holds 0 and everything below
+// 2^-30; the last bin everything above).  The top 11 bits of the pattern would
+// give 4 bins per octave, so that a row's scores, which span a few octaves,
+// fall into about a dozen bins: the shared-memory atomics of the histogram
+// then serialise on those bins, and the boundary bin holds several times more
+// candidates.
+constexpr int kFirstShift = 18;               // 23 - 5 mantissa bits: 32 bins per octave
+constexpr int kFirstBase = 97 << 5;           // (biased exponent of 2^-30) x 32
+__device__ __forceinline__ int first_bin(uint32_t u) {
+  const int b = (int)(u >> kFirstShift) - kFirstBase;
+  return b < 0 ? 0 : (b > kSelBins - 1 ? kSelBins - 1 : b);
+}
+__device__ __forceinline__ uint32_t first_bin_lo(int b) {
+  return b == 0 ? 0u : (uint32_t)(b + kFirstBase) << kFirstShift;
+}
+__device__ __forceinline__ uint32_t first_bin_hi(int b) {
+  return b == kSelBins - 1 ? 0x7fffffffu : ((uint32_t)(b + kFirstBase + 1) << kFirstShift) - 1u;
+}
+
 template <int kSelCluster>
 __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelThreads)
 topk_select_cluster_kernel(const float* __restrict__ S, int64_t s_stride, const int64_t* __restrict__ q_pos,
@@ -368,7 +389,7 @@ topk_select_cluster_kernel(const float* __restrict__ S, int64_t s_stride, const 
     load_batch(b0, u);
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (u[j] != 0xffffffffu) atomicAdd(&sm.base.hist[u[j] >> 20], 1);
+      if (u[j] != 0xffffffffu) atomicAdd(&sm.base.hist[first_bin(u[j])], 1);
   }
   cluster.sync();
   // The first CTA merges the histograms (this thread's bins summed over the
@@ -395,8 +416,8 @@ topk_select_cluster_kernel(const float* __restrict__ S, int64_t s_stride, const 
       for (int j = 0; j < kSelBinsPerThread; ++j) {
         if (above + loc[j] >= k_b) {
           const int bin = base_bin + kSelBinsPerThread - 1 - j;
-          sm.base.lo = (uint32_t)bin << 20;
-          sm.base.hi = ((uint32_t)bin << 20) | 0xfffffu;
+          sm.base.lo = first_bin_lo(bin);
+          sm.base.hi = first_bin_hi(bin);
           sm.base.need = k_b - above;
           sm.base.done = above + loc[j];  // entries at or above the bin, whole row
           break;

@@ -264,6 +264,39 @@ def test_exact_ties_take_lowest_block_ids():
         np.testing.assert_array_equal(gpu["idx"][0, j, :len(want)], want)
 
 
+@pytest.mark.parametrize("group,seed", [(3, 21), (40, 22)])
+def test_tied_key_groups_keep_their_lowest_blocks(group, seed):
+    """Indexer keys equal over groups of consecutive blocks, and zero in the
+    rotated dims, so that blocks of one group score exactly alike at every
+    query position.  A row that keeps part of a group must keep the group's
+    lowest block ids (research-hub notes, Key ideas, top-k_B bullet; ties go to
+    the lower block id).  Groups of 3 leave a short tied run at the k_B-th
+    score; groups of 40 leave a tied run longer than a warp."""
+    spec, wl = small_case(8192, 512, seed=seed)
+    cfg = cfg_for(spec)
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    nb = spec.n // spec.r
+    gv = torch.randn((nb + group - 1) // group, 64, generator=g)
+    keys = torch.zeros(spec.n, 128)
+    keys[:, 64:] = gv.repeat_interleave(group, 0)[:nb].repeat_interleave(spec.r, 0)
+    wl["k_idx"][0] = keys.to(torch.bfloat16).to(DEV)
+    gpu = run_prefill(cfg, wl)
+    selecting = spec.n - spec.r * (cfg.k_b + 1) + 1  # rows with c > k_B
+    assert gpu["fallback_rows"] < selecting // 2  # most rows went through the entry buffers
+    split = 0
+    for i in range(spec.n):
+        sel = gpu["idx"][0, i, :gpu["count"][0, i]]
+        later = sel[sel % group != 0]  # members after their group's first block
+        assert np.isin(later - 1, sel).all(), i  # each keeps the member before it
+        cut = ((sel + 1) % group != 0) & (sel + 1 < O.visible_blocks(i, spec.r)) & ~np.isin(sel + 1, sel)
+        split += int(cut.sum())
+    assert split > 0  # some rows cut a visible group at the k_B-th score
+    rows = QC.sample_rows(spec.n, cfg.k_b, spec.r, [], 120, seed)
+    res = QC.oracle_rows(wl, rows, cfg=cfg)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, cfg.r)
+    assert st["exact"] >= len(rows) - 1, st
+
+
 def test_planted_block_always_selected():
     """A key block equal to a row's query direction outranks every random block."""
     spec, wl = small_case(2048, 256, seed=9)
@@ -554,6 +587,32 @@ def test_decode_ignores_nonfinite_workspace_contents():
     idx, cnt = dec.idx.view(B, -1).cpu().numpy(), dec.count.view(B).cpu().numpy()
     for bb in range(B):
         check_decode_seq(cfg, wl, bb, idx, cnt, o, lse)
+
+
+def test_decode_tied_and_extreme_scores_select_exactly():
+    """Decode rows built to stress the top-k's first pass, which bins scores at
+    1/32 octave over [2^-30, 2^34): sequence 0 has compressed keys equal over
+    groups of 3 blocks and sequence 1 over groups of 40 (zero in the rotated
+    dims, so a group's blocks score exactly alike and ties go to the lower block
+    id), sequence 2 has all-zero keys (every score 0: the first k_B blocks win,
+    through the whole-row path since 5000 blocks tie), and sequence 3 keys
+    scaled by 2^-45 .. 2^40, so that its scores run past both clamped ends."""
+    spec = DecodeSpec("d", batch=4, ctx=20000, k_tokens=2048, seed=24)
+    wl = make_decode(spec, DEV)
+    g = torch.Generator(device="cpu").manual_seed(24)
+    nb = wl["n_blocks"]
+    kb = torch.zeros(4, nb, 128)
+    for bb, group in ((0, 3), (1, 40)):
+        gv = torch.randn((nb + group - 1) // group, 64, generator=g)
+        kb[bb, :, 64:] = gv.repeat_interleave(group, 0)[:nb]
+    scale = torch.exp2(torch.randint(-45, 41, (nb, 1), generator=g).float())
+    kb[3] = torch.randn(nb, 128, generator=g) * scale
+    wl["kbar"] = kb.to(torch.bfloat16).to(DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode(cfg, wl)
+    np.testing.assert_array_equal(idx[2], np.arange(cfg.k_b))
+    for bb in range(4):
+        assert check_decode_seq(cfg, wl, bb, idx, cnt, out, lse) == "exact", bb
 
 
 @pytest.mark.slow
