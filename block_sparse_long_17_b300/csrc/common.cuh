@@ -83,6 +83,12 @@ inline cudaError_t current_sm_count(int* sms) {
 // previous work on the stream was not a kernel launched this way).  This hides
 // the launch gap between the short kernels of a decode step.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream, if it was launched with
+// launch_dependent(), start now and run beside this one (once every CTA of this
+// grid has called it or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,

@@ -73,8 +73,7 @@ constexpr int kFMaxKb = 512;             // largest k_B the fused path handles
 constexpr int kFMaxCtas = 160;           // >= SM count; sizes the buffers
 constexpr int kFMinRows = 64;            // fewer query rows per sequence: scan path
 constexpr int kFbCtas = 148;             // fallback kernel CTAs (one row each at a time)
-constexpr int kTilesPerLaunch = 1024;    // tiles per fused launch (bounds the row buffers: 1.9 GiB)
-constexpr int kFinKWarps = 4;            // warps per CTA of the finalize kernel
+constexpr int kTilesPerLaunch = 1024;    // tiles per fused launch (bounds the row buffers: 1.9 GiB each)
 constexpr uint32_t kABytes = kMB * 128 * 2;     // 32 KB
 
 // Tile shape for H indexer heads: TT query tokens, NR = TT H MMA columns
@@ -429,6 +428,10 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* const smem_base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   FusedSmem& S = *reinterpret_cast<FusedSmem*>(smem_base);
+  // The finalize of the previous launch's range is launched dependent on this
+  // kernel: it may start now, on the registers and shared memory this CTA
+  // leaves free on its SM.  It reads only the other entry buffer.
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &S.abort_flag;
   const int64_t rounds = (t_count + gridDim.x - 1) / gridDim.x;
@@ -762,18 +765,21 @@ index_topk_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 // exact top-k_B of the entries their tile collected (finalize_row), or are
 // queued for the exact fallback kernel when their buffer fell outside
 // [k_B, kFCap] entries or a segment overflowed.
-template <int TT>
-__global__ void __launch_bounds__(32 * kFinKWarps, 4)
+// W warps per CTA: 4 (four CTAs per SM) for a finalize that has the GPU to
+// itself; 2 (8192 registers) for one that runs beside a fused launch, whose CTA
+// leaves exactly that many registers of its SM free.
+template <int TT, int W>
+__global__ void __launch_bounds__(32 * W, 16 / W)
 index_finalize_kernel(const uint2* __restrict__ buf, const int* __restrict__ cnt, const int64_t* __restrict__ q_pos,
                       int64_t n_q, int tiles_per_seq, int t_begin, int t_count, int rshift, int k_b,
                       int64_t c_cap, int32_t* __restrict__ idx, int32_t* __restrict__ count,
                       int64_t* __restrict__ fb_rows, int* __restrict__ fb_count) {
   constexpr int tt = TT;
-  __shared__ __align__(16) uint32_t hist[kFinKWarps][512];
-  __shared__ int32_t ids[kFinKWarps][kFCap];
+  __shared__ __align__(16) uint32_t hist[W][512];
+  __shared__ int32_t ids[W][kFCap];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = t_count * tt;  // tt: tokens per tile; 32-bit row and tile indices
-  for (int rr = blockIdx.x * kFinKWarps + w; rr < rows; rr += gridDim.x * kFinKWarps) {
+  for (int rr = blockIdx.x * W + w; rr < rows; rr += gridDim.x * W) {
     const int lt = rr / tt;
     const int t = rr - lt * tt;
     const int tile = t_begin + lt;
@@ -878,13 +884,17 @@ index_fallback_kernel(const __nv_bfloat16* __restrict__ qt, const __nv_bfloat16*
 
 struct FusedLayout {
   int64_t tiles_per_seq, n_tiles, tiles_per_launch;
+  int nbuf;                   // entry buffers: 2 when there is more than one launch
+  int64_t buf_elems, cnt_elems;  // per buffer
   size_t buf_off, cnt_off, fb_rows_off, fb_count_off, scratch_off, total;
   int64_t scratch_stride;
 };
 
 // Workspace of the fused path (after the rotated queries): the entry buffers of
 // one launch's tiles (48 or 24 tokens x 4 segments x kSeg entries per tile) and their
-// counts, the fallback row list and counter, and the fallback kernel's score rows.
+// counts, twice when the tiles take several launches (launch j fills buffer
+// j % 2 while the finalize of launch j - 1 reads the other), the fallback row
+// list and counter, and the fallback kernel's score rows.
 inline FusedLayout fused_layout(int64_t B, int64_t n_q, int64_t n_blocks_max, int H) {
   auto al = [](size_t x) { return (x + 255) / 256 * 256; };
   const int tt = fused_tile_tokens(H);
@@ -892,9 +902,12 @@ inline FusedLayout fused_layout(int64_t B, int64_t n_q, int64_t n_blocks_max, in
   L.tiles_per_seq = (n_q + tt - 1) / tt;
   L.n_tiles = B * L.tiles_per_seq;
   L.tiles_per_launch = L.n_tiles < kTilesPerLaunch ? L.n_tiles : kTilesPerLaunch;
+  L.nbuf = L.n_tiles > L.tiles_per_launch ? 2 : 1;
+  L.buf_elems = L.tiles_per_launch * tt * 4 * kSeg;
+  L.cnt_elems = L.tiles_per_launch * 4 * tt;
   L.buf_off = 0;
-  L.cnt_off = al(L.buf_off + (size_t)L.tiles_per_launch * tt * 4 * kSeg * sizeof(uint2));
-  L.fb_rows_off = al(L.cnt_off + (size_t)L.tiles_per_launch * 4 * tt * sizeof(int));
+  L.cnt_off = al(L.buf_off + (size_t)L.nbuf * L.buf_elems * sizeof(uint2));
+  L.fb_rows_off = al(L.cnt_off + (size_t)L.nbuf * L.cnt_elems * sizeof(int));
   L.fb_count_off = al(L.fb_rows_off + (size_t)B * n_q * sizeof(int64_t));
   L.scratch_off = al(L.fb_count_off + sizeof(int));
   L.scratch_stride = (n_blocks_max + 63) / 64 * 64;
@@ -917,6 +930,31 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
   return fn;
+}
+
+// One finalize launch over tiles [t_begin, t_begin + t_count) (tile and row
+// indices of a launch fit 32 bits: at most kTilesPerLaunch tiles).  dependent:
+// launched with launch_dependent() behind the next range's fused launch (the
+// kernel does not wait for that launch: what it reads was written by the one
+// before, which the stream order has finished).
+template <int TT, int W>
+static cudaError_t launch_finalize(bool dependent, const uint2* buf, const int* cnt, const int64_t* q_pos,
+                                   int64_t n_q, int64_t tiles_per_seq, int64_t t_begin, int64_t t_count, int rshift,
+                                   int k_b, int64_t c_cap, int32_t* idx, int32_t* count, int64_t* fb_rows,
+                                   int* fb_count, cudaStream_t st) {
+  const unsigned grid = (unsigned)((t_count * TT + W - 1) / W);
+  if (!dependent) {
+    index_finalize_kernel<TT, W><<<grid, 32 * W, 0, st>>>(buf, cnt, q_pos, n_q, (int)tiles_per_seq, (int)t_begin,
+                                                          (int)t_count, rshift, k_b, c_cap, idx, count, fb_rows,
+                                                          fb_count);
+    return count_launch(cudaGetLastError());
+  }
+  // All of the SM's unified storage as shared memory, as the fused CTA beside it has set.
+  cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(index_finalize_kernel<TT, W>), 0);
+  if (e != cudaSuccess) return e;
+  return count_launch(launch_dependent(index_finalize_kernel<TT, W>, dim3(grid), dim3(32 * W), 0, st, buf, cnt,
+                                       q_pos, n_q, (int)tiles_per_seq, (int)t_begin, (int)t_count, rshift, k_b,
+                                       c_cap, idx, count, fb_rows, fb_count));
 }
 
 cudaError_t launch_index_fused(int H, const __nv_bfloat16* qt, const __nv_bfloat16* kbar, int64_t kbar_stride_b,
@@ -991,15 +1029,24 @@ cudaError_t launch_index_fused(int H, const __nv_bfloat16* qt, const __nv_bfloat
   if (e != cudaSuccess) return e;
   int rshift = 0;  // r is a power of two
   while ((1 << rshift) < r) ++rshift;
-  // Launches over ranges of tiles, the last (heaviest) range first.
-  for (int64_t t_end = L.n_tiles; t_end > 0; t_end -= L.tiles_per_launch) {
+  // Launches over ranges of tiles, the last (heaviest) range first.  The
+  // finalize of range j is launched after the fused launch of range j + 1,
+  // dependent on it, and runs beside it (two-warp CTAs on the registers the
+  // fused CTAs leave free, then on whole SMs once that launch drains); the
+  // fused launch of range j + 2 waits for both.  The finalize of the last
+  // range follows it alone, in four-warp CTAs.
+  int64_t p_begin = 0, p_count = 0;  // range waiting for its finalize
+  int p_half = 0, half = 0;
+  for (int64_t t_end = L.n_tiles; t_end > 0; t_end -= L.tiles_per_launch, half ^= 1) {
     const int64_t t_begin = t_end > L.tiles_per_launch ? t_end - L.tiles_per_launch : 0;
     const int64_t t_count = t_end - t_begin;
     int64_t grid = sms < kFMaxCtas ? sms : kFMaxCtas;
     if (grid > t_count) grid = t_count;
+    uint2* const hbuf = buf + half * L.buf_elems;
+    int* const hcnt = cnt + half * L.cnt_elems;
 #define QSA_FUSED_LAUNCH(HH)                                                                                 \
   index_topk_fused_kernel<HH><<<(unsigned)grid, kFThreads, kFusedSmemBytes, st>>>(                           \
-      tm_q, tm_k, tm_kp, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, aim, n_blocks_max, buf, cnt)
+      tm_q, tm_k, tm_kp, q_pos, n_q, L.tiles_per_seq, t_begin, t_count, rshift, k_b, aim, n_blocks_max, hbuf, hcnt)
     switch (H) {
       case 1: QSA_FUSED_LAUNCH(1); break;
       case 2: QSA_FUSED_LAUNCH(2); break;
@@ -1009,17 +1056,26 @@ cudaError_t launch_index_fused(int H, const __nv_bfloat16* qt, const __nv_bfloat
 #undef QSA_FUSED_LAUNCH
     e = count_launch(cudaGetLastError());
     if (e != cudaSuccess) return e;
-    const int64_t fin_blocks = (t_count * tt + kFinKWarps - 1) / kFinKWarps;
-    // Tile and row indices of a launch fit 32 bits (at most kTilesPerLaunch tiles).
-    if (tt == 48)
-      index_finalize_kernel<48><<<(unsigned)fin_blocks, 32 * kFinKWarps, 0, st>>>(
-          buf, cnt, q_pos, n_q, (int)L.tiles_per_seq, (int)t_begin, (int)t_count, rshift, k_b, n_blocks_max, idx,
-          count, fb_rows, fb_count);
-    else
-      index_finalize_kernel<24><<<(unsigned)fin_blocks, 32 * kFinKWarps, 0, st>>>(
-          buf, cnt, q_pos, n_q, (int)L.tiles_per_seq, (int)t_begin, (int)t_count, rshift, k_b, n_blocks_max, idx,
-          count, fb_rows, fb_count);
-    e = count_launch(cudaGetLastError());
+    if (p_count > 0) {
+      e = tt == 48 ? launch_finalize<48, 2>(true, buf + p_half * L.buf_elems, cnt + p_half * L.cnt_elems, q_pos,
+                                            n_q, L.tiles_per_seq, p_begin, p_count, rshift, k_b, n_blocks_max, idx,
+                                            count, fb_rows, fb_count, st)
+                   : launch_finalize<24, 2>(true, buf + p_half * L.buf_elems, cnt + p_half * L.cnt_elems, q_pos,
+                                            n_q, L.tiles_per_seq, p_begin, p_count, rshift, k_b, n_blocks_max, idx,
+                                            count, fb_rows, fb_count, st);
+      if (e != cudaSuccess) return e;
+    }
+    p_begin = t_begin;
+    p_count = t_count;
+    p_half = half;
+  }
+  if (p_count > 0) {
+    e = tt == 48 ? launch_finalize<48, 4>(false, buf + p_half * L.buf_elems, cnt + p_half * L.cnt_elems, q_pos, n_q,
+                                          L.tiles_per_seq, p_begin, p_count, rshift, k_b, n_blocks_max, idx, count,
+                                          fb_rows, fb_count, st)
+                 : launch_finalize<24, 4>(false, buf + p_half * L.buf_elems, cnt + p_half * L.cnt_elems, q_pos, n_q,
+                                          L.tiles_per_seq, p_begin, p_count, rshift, k_b, n_blocks_max, idx, count,
+                                          fb_rows, fb_count, st);
     if (e != cudaSuccess) return e;
   }
   index_fallback_kernel<<<kFbCtas, kSelThreads, 0, st>>>(
