@@ -755,10 +755,11 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev) -> 
     """The same step through the binding with host buffers: H2D of the step's
     inputs from pinned memory and D2H of its outputs, all inside the timed
     region.  The prefill runs as chunked prefill (the pages' mode) over the
-    chunks of e2e_chunk_bounds: one stream copies chunk i in, one computes it
-    (compress its blocks, select and attend its rows against the prefix), one
-    copies its output back, so that the copies of one chunk overlap the kernels
-    of another.  The decode step runs first on the compute stream, while the
+    chunks of e2e_chunk_bounds: one stream copies chunk i in (the indexer's
+    inputs first), one computes it (compress its blocks and select its rows as
+    soon as those are in, attend its rows against the prefix once its q, K and
+    V are), one copies its output back, so that the copies of one chunk
+    overlap the kernels of another.  The decode step runs first on the compute stream, while the
     first chunk's inputs come in."""
     import torch
     host_in = {k: wl[k].cpu().pin_memory() for k in ("q_idx", "k_idx", "q", "k", "v")}
@@ -805,19 +806,26 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev) -> 
         with torch.cuda.stream(s_out):
             dout_h.copy_(dec.out, non_blocking=True)
         for i, (lo, hi) in enumerate(chunks):
+            # The indexer's inputs first, on their own event, so that the
+            # chunk's selection runs while its q, K and V rows (80% of its
+            # bytes) are still coming in; the attention waits for all of them.
             with torch.cuda.stream(s_in):
-                for key in ("k_idx", "q_idx", "q"):
+                for key in ("k_idx", "q_idx"):
                     dev_in[key][:, lo:hi].copy_(host_in[key][:, lo:hi], non_blocking=True)
+                idx_ready = torch.cuda.Event()
+                idx_ready.record(s_in)
+                dev_in["q"][:, lo:hi].copy_(host_in["q"][:, lo:hi], non_blocking=True)
                 for key in ("k", "v"):
                     for g in range(hkv):
                         dev_in[key][0, g, lo:hi].copy_(host_in[key][0, g, lo:hi], non_blocking=True)
                 ready = torch.cuda.Event()
                 ready.record(s_in)
-            s_cmp.wait_event(ready)
+            s_cmp.wait_event(idx_ready)
             b0, b1 = lo // r, hi // r
             qsa.qsa_compress_keys(cfg, dev_in["k_idx"], b0, b1 - b0, pre.kbar, stream=s_cmp)
             qsa.qsa_index_topk(cfg, dev_in["q_idx"][:, lo:hi], pre.kbar, qpos[i], b1, pre.idx[:, lo:hi],
                                pre.count[:, lo:hi], ws_c, stream=s_cmp)
+            s_cmp.wait_event(ready)
             qsa.qsa_sparse_attn_prefill(cfg, dev_in["q"][:, lo:hi], dev_in["k"], dev_in["v"], qpos[i],
                                         pre.idx[:, lo:hi], pre.count[:, lo:hi], pre.out[:, lo:hi],
                                         pre.lse[:, lo:hi], stream=s_cmp)
