@@ -18,12 +18,15 @@ constexpr int kCompressWarps = 8;
 // l / 16 + 2, ..., and the two half-warps add their sums.  The pooled fp32 row
 // is staged in shared memory so that any even rope_dims can pair dim j with
 // dim j + rope_dims/2; lane l then rotates and stores dims 4 l .. 4 l + 3
-// (one 256-byte store per warp).
+// (one 256-byte store per warp).  The angle of pair j (reduced in fp64,
+// whose rate on this GPU is low) is computed once, by lane j % 32, into
+// shared memory.
 __global__ void __launch_bounds__(kCompressWarps * 32)
 compress_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_t k_stride_b, int64_t B,
                      int64_t first_block, int64_t n_blocks, int r, int rmsnorm, float rms_eps,
                      RopeParams rope, __nv_bfloat16* __restrict__ kbar, int64_t kbar_stride_b) {
   __shared__ __align__(16) float pooled[kCompressWarps][kHeadDim];
+  __shared__ float cs[kCompressWarps][2][kMaxRopePairs];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t item = (int64_t)blockIdx.x * kCompressWarps + warp;
   if (item >= B * n_blocks) return;
@@ -31,6 +34,13 @@ compress_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_t k_stride_b
   const int64_t blk = first_block + item % n_blocks;
   const __nv_bfloat16* src = k_idx + bb * k_stride_b + blk * r * kHeadDim;
   const int chunk = lane & 15;
+  const int half = rope.half;
+  for (int j = lane; j < half; j += 32) {
+    float c, sn;
+    rope_cos_sin(blk, rope.theta[j], &c, &sn);
+    cs[warp][0][j] = c;
+    cs[warp][1][j] = sn;
+  }
 
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int t = lane >> 4; t < r; t += 2) {
@@ -62,7 +72,6 @@ compress_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_t k_stride_b
   }
   __syncwarp();
 
-  const int half = rope.half;
   float y[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
@@ -70,8 +79,7 @@ compress_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_t k_stride_b
     y[u] = pooled[warp][dim];
     if (dim < 2 * half) {
       const int j = dim < half ? dim : dim - half;
-      float c, s;
-      rope_cos_sin(blk, rope.theta[j], &c, &s);
+      const float c = cs[warp][0][j], s = cs[warp][1][j];
       const float x1 = pooled[warp][j], x2 = pooled[warp][j + half];
       y[u] = dim < half ? fmaf(x1, c, -x2 * s) : fmaf(x1, s, x2 * c);
     }
@@ -81,17 +89,29 @@ compress_keys_kernel(const __nv_bfloat16* __restrict__ k_idx, int64_t k_stride_b
 }
 
 // One warp per query token: the RoPE angles of position floor(i / r) are
-// computed once per token and applied to all n_heads indexer heads.
+// computed once per token and applied to all n_heads indexer heads.  The
+// token's rows (n_heads x 256 bytes) are loaded up front, 16 bytes per lane
+// and load, together with its position, so that the warp waits for one
+// round trip to memory rather than one per head; they are staged as fp32 in
+// shared memory, and lane l rotates and stores dims l + 32 u of each head.
 __global__ void __launch_bounds__(kCompressWarps * 32)
 rotate_queries_kernel(const __nv_bfloat16* __restrict__ q_idx, const int64_t* __restrict__ q_pos,
                       int64_t B, int64_t n_q, int r, int n_heads, RopeParams rope,
                       __nv_bfloat16* __restrict__ qt) {
+  constexpr int kVecPerHead = kHeadDim / 8;                      // 16-byte vectors per head row
+  constexpr int kMaxVec = kMaxIdxHeads * kVecPerHead / 32;       // per lane
   __shared__ float cs[kCompressWarps][2][kMaxRopePairs];
-  __shared__ float row[kCompressWarps][kHeadDim];
+  __shared__ __align__(16) float rows[kCompressWarps][kMaxIdxHeads * kHeadDim];
   griddep_wait();  // launched dependent: the previous kernel may still write its inputs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t item = (int64_t)blockIdx.x * kCompressWarps + warp;
   if (item >= B * n_q) return;
+  const int nvec = n_heads * kVecPerHead;
+  const uint4* src = reinterpret_cast<const uint4*>(q_idx + item * (n_heads * kHeadDim));
+  uint4 v[kMaxVec];
+#pragma unroll
+  for (int u = 0; u < kMaxVec; ++u)
+    if (lane + 32 * u < nvec) v[u] = ldg_stream(src + lane + 32 * u);
   const int64_t bb = item / n_q;
   const int64_t pos = (q_pos[bb] + item % n_q) / r;
   const int half = rope.half;
@@ -101,21 +121,28 @@ rotate_queries_kernel(const __nv_bfloat16* __restrict__ q_idx, const int64_t* __
     cs[warp][0][j] = c;
     cs[warp][1][j] = s;
   }
-  const __nv_bfloat16* src = q_idx + item * (n_heads * kHeadDim);
+  float* const row = rows[warp];
+#pragma unroll
+  for (int u = 0; u < kMaxVec; ++u) {
+    const int e = lane + 32 * u;  // dims 8 e .. 8 e + 7 of the token's concatenated head rows
+    if (e < nvec) {
+      float4* d = reinterpret_cast<float4*>(row + 8 * e);
+      d[0] = make_float4(bf16_lo(v[u].x), bf16_hi(v[u].x), bf16_lo(v[u].y), bf16_hi(v[u].y));
+      d[1] = make_float4(bf16_lo(v[u].z), bf16_hi(v[u].z), bf16_lo(v[u].w), bf16_hi(v[u].w));
+    }
+  }
+  __syncwarp();
   __nv_bfloat16* dst = qt + item * (n_heads * kHeadDim);
   for (int h = 0; h < n_heads; ++h) {
-    __syncwarp();
-#pragma unroll
-    for (int u = 0; u < 4; ++u) row[warp][lane + 32 * u] = __bfloat162float(src[h * kHeadDim + lane + 32 * u]);
-    __syncwarp();
+    const float* hrow = row + h * kHeadDim;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int dim = lane + 32 * u;
-      float y = row[warp][dim];
+      float y = hrow[dim];
       if (dim < 2 * half) {
         const int j = dim < half ? dim : dim - half;
         const float c = cs[warp][0][j], s = cs[warp][1][j];
-        const float x1 = row[warp][j], x2 = row[warp][j + half];
+        const float x1 = hrow[j], x2 = hrow[j + half];
         y = dim < half ? fmaf(x1, c, -x2 * s) : fmaf(x1, s, x2 * c);
       }
       dst[h * kHeadDim + dim] = __float2bfloat16_rn(y);
