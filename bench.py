@@ -562,9 +562,10 @@ def main():
         dwl = make_decode(dspec, dev)
         dec = qsa.QsaDecode(dcfg, dspec.batch, dwl["n_blocks"], dspec.hq, dspec.hkv, device=dev)
         dq = dwl["q"][:, 0].contiguous()
+        dq_pos = dwl["cache_lens"] - 1  # the new token's position: decode state, like the caches
     else:
         dwl = {"cache_len": dspec.cache_len}
-        dec = dq = None
+        dec = dq = dq_pos = None
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     names = ["compress", "index_prefill", "attn_prefill", "index_decode", "attn_decode"]
@@ -579,8 +580,7 @@ def main():
                                     pre.out, pre.lse)
         evs[3].record(stream)
         if do_decode:
-            q_pos = dwl["cache_lens"] - 1
-            qsa.qsa_index_topk(dcfg, dwl["q_idx"], dwl["kbar"], q_pos, dwl["n_blocks"], dec.idx, dec.count,
+            qsa.qsa_index_topk(dcfg, dwl["q_idx"], dwl["kbar"], dq_pos, dwl["n_blocks"], dec.idx, dec.count,
                                dec.ws_idx)
         evs[4].record(stream)
         if do_decode:
@@ -767,6 +767,7 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev) -> 
     dq_h = dwl["q"][:, 0].contiguous().cpu().pin_memory()
     dqi_h = dwl["q_idx"].cpu().pin_memory()
     dq_d, dqi_d = torch.empty_like(dq_h, device=dev), torch.empty_like(dqi_h, device=dev)
+    dq_pos = dwl["cache_lens"] - 1  # decode state (positions), device-resident like the caches
     out_h = torch.empty(pre.out.shape, dtype=pre.out.dtype).pin_memory()
     dout_h = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values()) + dq_h.numel() * 2 + dqi_h.numel() * 2
@@ -795,8 +796,7 @@ def e2e_measure(qsa, cfg, dcfg, wl, dwl, pre, dec, dspec, args, stream, dev) -> 
         # The decode step needs none of the prefill: it runs first, while the
         # first chunk's inputs are still coming in.
         s_cmp.wait_event(dec_in)
-        q_pos = dwl["cache_lens"] - 1
-        qsa.qsa_index_topk(dcfg, dqi_d, dwl["kbar"], q_pos, dwl["n_blocks"], dec.idx, dec.count, dec.ws_idx,
+        qsa.qsa_index_topk(dcfg, dqi_d, dwl["kbar"], dq_pos, dwl["n_blocks"], dec.idx, dec.count, dec.ws_idx,
                            stream=s_cmp)
         qsa.qsa_sparse_attn_decode(dcfg, dq_d, dwl["k"], dwl["v"], dwl["cache_lens"], dec.idx.view(dspec.batch, -1),
                                    dec.count.view(dspec.batch), dec.out, dec.ws_attn, dec.lse, stream=s_cmp)
