@@ -445,6 +445,24 @@ def test_indexer_head_counts_prefill_fused_path(h_idx):
     assert st["exact"] >= 0.98 * len(rows), st
 
 
+def test_eight_head_prefill_across_launch_ranges():
+    """8 indexer heads (24-token tiles) over 53248 rows: 2219 tiles in three
+    fused launches of at most 1024 tiles, heaviest first ([1195, 2219),
+    [171, 1195), [0, 171)), the finalize of the first two running beside the
+    next launch from the other entry buffer.  Whole tiles on both sides of
+    each seam, the first and the last tile, and sampled rows match the oracle."""
+    spec = PrefillSpec("h8", n=53248, k_tokens=2048, seed=68, h_idx=8)
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    gpu = run_prefill(cfg, wl)
+    tiles = [0, 170, 171, 1194, 1195, 2218]  # the last tile holds rows 53232 .. 53247 only
+    rows = sorted({24 * t + j for t in tiles for j in range(24) if 24 * t + j < spec.n}
+                  | set(QC.sample_rows(spec.n, cfg.k_b, spec.r, [], 40, 68)))
+    res = QC.oracle_rows(wl, rows, cfg=cfg)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, cfg.r)
+    assert st["exact"] >= len(rows) - 2, st
+
+
 @pytest.mark.parametrize("h_idx", [1, 2, 8])
 def test_indexer_head_counts_scan_path(h_idx):
     """A 40-row chunk (fewer than 64 rows: the one-pass scan path, 8 / H rows per
