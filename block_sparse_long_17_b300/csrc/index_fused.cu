@@ -120,9 +120,12 @@ struct TileMeta {
 constexpr int kPilotStride = 16;   // the pilot samples every 16th block (per phase)
 // At least this many pilot samples per row when possible: with the aim below
 // about 50 samples are expected above a row's threshold at every context
-// length.  (2048 spent 15% of the 128K indexer's chunks on the pilot and sent
-// no fewer rows to the fallback: 1024 is 4% faster there.)
-constexpr int kPilotMin = 1024;
+// length (one phase of every 16th block gives c / 16 samples, and aim / 16 of
+// them above).  Measured at 128K and 32K: 1024 took 1% and 5% longer (more
+// phases for rows below 16384 visible blocks); 384 or 256 sent one or two of
+// the 32K rows to the exact fallback, whose full-row scoring cost more than
+// the pilot saved; 2048 spent 15% of the 128K chunks on the pilot.
+constexpr int kPilotMin = 512;
 // tau aims at sqrt(k_B kFCap) entries per row, the middle in ratio of the
 // accepted [k_B, kFCap]: 1.6 k_B at k_B = 512, 3.2 k_B at k_B = 128, where the
 // quantile sought lies further in the tail and the pilot's estimate of it is

@@ -310,11 +310,12 @@ def test_planted_block_always_selected():
 
 
 def test_unsampled_high_blocks_take_the_exact_fallback():
-    """Rows that see 4096 blocks are pilot-sampled at block residues 0..11 (mod
-    16).  Here only blocks of residues 12..15 score high, so those rows'
-    thresholds come from the low scores, they collect more entries than their
-    buffer holds, and the exact full-row fallback must select them: the result
-    is still the oracle's."""
+    """Rows that see 3072 to 4096 blocks are pilot-sampled at the first few
+    block residues mod 16 (as many phases of every 16th block as reach the
+    pilot's minimum sample count: two or three).  Here only blocks of residues
+    12..15 score high, so those rows' thresholds come from the low scores,
+    they collect more entries than their buffer holds, and the exact full-row
+    fallback must select them: the result is still the oracle's."""
     spec, wl = small_case(16384, 2048, seed=11)
     cfg = cfg_for(spec)
     g = torch.Generator(device="cpu").manual_seed(11)
