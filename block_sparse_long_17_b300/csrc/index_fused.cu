@@ -129,8 +129,8 @@ constexpr int kPilotMin = 512;
 // tau aims at sqrt(k_B kFCap) entries per row, the middle in ratio of the
 // accepted [k_B, kFCap]: 1.6 k_B at k_B = 512, 3.2 k_B at k_B = 128, where the
 // quantile sought lies further in the tail and the pilot's estimate of it is
-// noisier
-// (never below 1.6 k_B).
+// noisier (never below 1.6 k_B).  Aims of 0.92 and 0.85 times this sent 49
+// and 620 of the 128K rows to the exact fallback (4% and 18% slower).
 inline int pilot_aim(int k_b) {
   const double g = std::sqrt((double)k_b * kFCap), lo = 1.6 * k_b;
   return (int)((g > lo ? g : lo) + 0.5);
