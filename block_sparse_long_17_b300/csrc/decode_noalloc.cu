@@ -22,8 +22,9 @@
 namespace qsa {
 
 // QSA_NOALLOC_SCRATCH_BYTES (32 MiB): enough for the partials of 64 sequences x
-// 2 kv heads at K = 2048, r = 4 (room for 17 splits of 128 tokens, 4160 B per
-// split and head chunk, plus a completion counter per head chunk: 9 MB).
+// 2 kv heads at K = 2048, r = 4 (room for 11 splits of at least 192 tokens,
+// 4160 B per split and head chunk, plus a completion counter per head chunk:
+// 6 MB).
 constexpr size_t kNoAllocScratchBytes = QSA_NOALLOC_SCRATCH_BYTES;
 constexpr int kNoAllocMaxDevices = 64;
 

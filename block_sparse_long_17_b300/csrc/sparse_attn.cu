@@ -394,7 +394,8 @@ sparse_attn_prefill_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloa
 // (fp32) with its running max and sum per head, then counts itself in the
 // unit's counter; the warp that completes the count combines the unit's
 // splits (log-sum-exp weights) into the bf16 output and resets the counter.
-constexpr int kDecodeMinSplit = 128;  // fewest slots per split (64 was slower: more partials to combine)
+constexpr int kDecodeMinSplit = 192;  // fewest slots per split (4 x 1M, next_n = 4: 192 or 256 took
+                                      // 28.7 us, 128 30.8 us, 64 41 us: every split adds a partial to combine)
 
 // Combine of one (sequence, kv head, head chunk) by one warp.  Lane L owns
 // dims 4L .. 4L + 3 of all 8 heads; every lane reads the splits' maxima and
