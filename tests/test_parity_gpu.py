@@ -430,6 +430,32 @@ def test_batched_prefill_sequences_at_different_offsets(impl):
     assert exact >= 3 * len(rows) - 1
 
 
+def test_batched_prefill_across_launch_ranges():
+    """Three whole 20000-row sequences in one call: 3 x 417 tiles, launched as
+    the ranges [227, 1251) and [0, 227), so the seam falls inside sequence 0
+    and the sequence boundaries (tiles 416 | 417 and 833 | 834) inside the
+    first launch, and the first range's finalize reads its entry buffer beside
+    the second launch.  Whole tiles at the seam and at every sequence's ends
+    match the oracle run on that sequence alone."""
+    spec = PrefillSpec("b3r", n=20000, k_tokens=2048, seed=52, batch=3)
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    gpu = run_prefill(cfg, wl)
+    last = range(19968, 20000)  # local tile 416 holds 32 rows
+    rows_of = {0: list(range(48)) + list(range(226 * 48, 228 * 48)) + list(last),
+               1: list(range(48)) + list(last),
+               2: list(range(48)) + list(last)}
+    exact = total = 0
+    for b, rows in rows_of.items():
+        rows = sorted(set(rows) | set(QC.sample_rows(spec.n, cfg.k_b, spec.r, [], 12, 52 + b)))
+        one = {k: wl[k][b:b + 1] for k in ("q_idx", "k_idx", "q", "k", "v")}
+        res = QC.oracle_rows(one, rows, cfg=cfg)
+        st = QC.compare_prefill(res, gpu["idx"][b], gpu["count"][b], gpu["out"][b], gpu["lse"][b], cfg.k_b, cfg.r)
+        exact += st["exact"]
+        total += len(rows)
+    assert exact >= total - 2, (exact, total)
+
+
 # ----------------------------------------------------------------------------- indexer head counts
 
 @pytest.mark.parametrize("h_idx", [1, 2, 8])
