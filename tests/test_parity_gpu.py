@@ -348,6 +348,25 @@ def test_chunked_prefill_rows_at_offset():
     assert st["exact"] >= 0.98 * (hi - lo)
 
 
+def test_offset_chunk_across_launch_ranges():
+    """A 51000-row chunk at positions 49000 .. 99999 of a 100000-token
+    sequence: 1063 tiles whose positions start at the chunk's offset, launched
+    as [39, 1063) then [0, 39).  Whole tiles at the seam and at both ends of
+    the chunk, and sampled rows, match the oracle."""
+    spec = PrefillSpec("oc", n=100000, k_tokens=2048, seed=53)
+    wl = make_prefill(spec, DEV)
+    cfg = cfg_for(spec)
+    lo, hi = 49000, 100000
+    gpu = run_prefill(cfg, wl, q_pos0=lo, rows=slice(lo, hi))
+    n_q = hi - lo
+    rows = set(range(48)) | set(range(38 * 48, 40 * 48)) | set(range(1062 * 48, n_q))
+    rows |= {int(x) for x in np.random.default_rng(53).integers(0, n_q, size=24)}
+    rows = sorted(rows)
+    res = QC.oracle_rows({**wl, "q_idx": wl["q_idx"][:, lo:hi], "q": wl["q"][:, lo:hi]}, rows, cfg=cfg, q_pos0=lo)
+    st = QC.compare_prefill(res, gpu["idx"][0], gpu["count"][0], gpu["out"][0], gpu["lse"][0], cfg.k_b, cfg.r)
+    assert st["exact"] >= len(rows) - 2, st
+
+
 def test_rows_per_wave_and_chunks_of_it_match_the_one_call_prefill():
     """qsa_index_rows_per_wave is the indexer's tile rows times the SM count.  A
     prefill run as chunks shaped like the end-to-end pipeline's (small chunks
