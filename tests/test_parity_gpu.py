@@ -621,6 +621,19 @@ def test_decode_small_matches_oracle(ctx):
     assert kinds.count("exact") >= 2
 
 
+@pytest.mark.parametrize("r,ctx", [(2, 3001), (8, 5003), (16, 9001)])
+def test_decode_other_block_sizes(r, ctx):
+    """Decode with micro-blocks of 2, 8 and 16 tokens: the scan's count of
+    visible blocks and the attention's expansion of the selected blocks and
+    of the tail (up to r - 1 tokens) depend on r."""
+    spec = DecodeSpec("dr", batch=3, ctx=ctx, k_tokens=512, seed=33 + r, r=r)
+    wl = make_decode(spec, DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode(cfg, wl)
+    kinds = [check_decode_seq(cfg, wl, bb, idx, cnt, out, lse) for bb in range(3)]
+    assert kinds.count("exact") >= 2
+
+
 def test_decode_ragged_cache_lengths():
     """Sequences of one batch at different lengths (each its own c_i and tail)."""
     spec = DecodeSpec("d", batch=4, ctx=3000, k_tokens=256, seed=22)
@@ -731,6 +744,18 @@ def test_multi_token_decode_matches_oracle(next_n, ctx):
     idx, cnt, out, lse = run_decode_multi(cfg, wl)
     exact = sum(check_decode_multi_seq(cfg, wl, bb, idx, cnt, out, lse)["exact"] for bb in range(3))
     assert exact >= 3 * next_n - 1
+
+
+@pytest.mark.parametrize("r", [2, 16])
+def test_multi_token_decode_other_block_sizes(r):
+    """next_n = 4 rows per sequence with micro-blocks of 2 and 16 tokens: the
+    rows' visible block counts and tails differ, by row, with r."""
+    spec = DecodeSpec("dmr", batch=3, ctx=6007, k_tokens=512, seed=35 + r, next_n=4, r=r)
+    wl = make_decode(spec, DEV)
+    cfg = cfg_for(spec)
+    idx, cnt, out, lse = run_decode_multi(cfg, wl)
+    exact = sum(check_decode_multi_seq(cfg, wl, bb, idx, cnt, out, lse)["exact"] for bb in range(3))
+    assert exact >= 3 * 4 - 1
 
 
 def test_multi_token_decode_ragged_cache_lengths():
